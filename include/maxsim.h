@@ -1,0 +1,209 @@
+/*
+ * maxsim.h -- C ABI of libmaxsim.so, late-interaction MaxSim scoring on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operator ("TileMaxSim: IO-Aware GPU MaxSim Scoring with Dimension
+ * Tiling and Fused Product Quantization", §1; "FLASH-MAXSIM: IO-Aware Fused
+ * Kernels for Late-Interaction Scoring", Abstract):
+ *
+ *     score(Q, D_b) = sum_{i < nq} max_{j < L_b} <q_i, d_j>
+ *
+ * for a query Q of nq token embeddings and a document D_b of L_b token
+ * embeddings, all of dimension d. Inputs are taken as given: the library
+ * does not normalise them (the "cosine" of the pages is the dot product of
+ * L2-normalised embeddings).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, row-major
+ *    and contiguous. The library allocates and frees no device memory;
+ *    where an operation needs scratch space the caller passes a workspace
+ *    sized by the matching *_workspace_size() query.
+ *  - Element pointers must be 16-byte aligned (TMA and vector loads).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Every call is asynchronous on that stream and returns as soon
+ *    as its kernels are enqueued; outputs are valid once the stream reaches
+ *    that point.
+ *  - Errors: argument problems found on the host return
+ *    MAXSIM_ERR_INVALID_ARG or MAXSIM_ERR_UNSUPPORTED before anything is
+ *    launched. A failed launch returns MAXSIM_ERR_CUDA. Problems found on
+ *    the device (inconsistent CSR offsets or lengths, a pipeline wait that
+ *    gave up) cannot be returned by the asynchronous call; the kernel
+ *    records them in a per-device status word, treats a bad document as
+ *    empty, and maxsim_device_status() reports them. No kernel traps, asserts
+ *    or spins without a bound. No C++ exception crosses this ABI.
+ *  - Outputs are fp32 (scores, gradients) or int32 (indices). An empty
+ *    document (L_b = 0) scores 0.0 and has argmax -1.
+ *  - The argmax of query token i in document b is the LOWEST doc-local token
+ *    index j attaining the maximum similarity.
+ */
+#ifndef MAXSIM_H_
+#define MAXSIM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum maxsim_status {
+    MAXSIM_OK = 0,
+    MAXSIM_ERR_INVALID_ARG = 1,  /* NULL/misaligned pointer, negative size, bad lengths/offsets */
+    MAXSIM_ERR_UNSUPPORTED = 2,  /* valid arguments this build does not handle (e.g. d % 64 != 0 on the tensor-core path) */
+    MAXSIM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    MAXSIM_ERR_TIMEOUT = 4,      /* a device pipeline wait gave up after its time bound */
+    MAXSIM_ERR_WORKSPACE = 5     /* workspace NULL or smaller than the size query returned */
+} maxsim_status;
+
+typedef enum maxsim_dtype {
+    MAXSIM_BF16 = 0,   /* bf16 in, fp32 accumulate (tcgen05 tensor cores) */
+    MAXSIM_FP16 = 1,   /* fp16 in, fp32 accumulate (tcgen05 tensor cores) */
+    MAXSIM_FP32 = 2    /* fp32 in, fp32 FFMA on the CUDA cores */
+} maxsim_dtype;
+
+/* Bits of the device status word (see maxsim_device_status). */
+#define MAXSIM_DEVERR_TIMEOUT    0x1u  /* a pipeline wait exceeded its time bound */
+#define MAXSIM_DEVERR_BAD_INPUT  0x2u  /* a document's offsets/length were out of range */
+
+/* Library version: major*10000 + minor*100 + patch. */
+int maxsim_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *maxsim_status_string(maxsim_status status);
+
+/*
+ * maxsim_device_status -- synchronises `stream`, then reads and clears the
+ * status word of the current device. *flags (may be NULL) receives the
+ * MAXSIM_DEVERR_* bits seen since the last call. Returns MAXSIM_ERR_TIMEOUT
+ * if the timeout bit was set, else MAXSIM_ERR_INVALID_ARG if the bad-input
+ * bit was set, else MAXSIM_OK (or MAXSIM_ERR_CUDA if the stream failed).
+ */
+maxsim_status maxsim_device_status(void *stream, unsigned int *flags);
+
+/*
+ * maxsim_score -- padded layout, one or more queries.
+ *
+ * Follows TileMaxSim §1 (operator), §2(1) (every document byte streamed
+ * from HBM once, the per-query-token maximum kept on chip), §2(2)
+ * (dimension tiling: partial dot products over d-chunks are summed before
+ * the maximum) and §5 (fixed-Nd padding with a length mask); FLASH-MAXSIM
+ * Figure 1 / Algorithm 2 (running maximum from -inf, only the scalar score
+ * written back).
+ *
+ *   Q          [n_queries, nq, d]  dtype
+ *   D          [B, nd, d]          dtype; document b's tokens are rows
+ *                                  0 .. L_b-1 of D[b]; rows L_b .. nd-1 are
+ *                                  never read by the tensor-core path beyond
+ *                                  a 32-row granule and never contribute
+ *   doc_len    [B] int32 or NULL   L_b (0 <= L_b <= nd); NULL means L_b = nd
+ *   out        [n_queries, B] fp32 out[q*B + b] = score(Q[q], D_b)
+ *   argmax_out [n_queries, B, nq] int32 or NULL
+ *
+ * Limits: nq >= 1, n_queries >= 1, nd >= 1, B >= 0 (B = 0 is a no-op).
+ * BF16/FP16: d % 64 == 0 and 64 <= d <= 1024. FP32: d % 4 == 0, d <= 1024.
+ */
+maxsim_status maxsim_score(const void *Q, int n_queries, int nq, int d,
+                           const void *D, int64_t B, int nd, const int32_t *doc_len,
+                           maxsim_dtype dtype, float *out, int32_t *argmax_out,
+                           void *stream);
+
+/*
+ * maxsim_score_varlen -- variable-length, padding-free documents in CSR
+ * form (FLASH-MAXSIM, Abstract: variable-length padding-free scoring;
+ * TileMaxSim §5: the padding waste it removes).
+ *
+ *   D_packed   [total_tokens, d] dtype; document b owns rows
+ *              offsets[b] .. offsets[b+1]-1
+ *   offsets    [B+1] int64, offsets[0] = 0, non-decreasing,
+ *              offsets[B] = total_tokens (checked on the device: a document
+ *              whose range falls outside [0, total_tokens] is scored as
+ *              empty and sets MAXSIM_DEVERR_BAD_INPUT)
+ *   out        [n_queries, B] fp32; argmax_out [n_queries, B, nq] int32 or NULL
+ *
+ * Same dtype and d limits as maxsim_score.
+ */
+maxsim_status maxsim_score_varlen(const void *Q, int n_queries, int nq, int d,
+                                  const void *D_packed, const int64_t *offsets,
+                                  int64_t B, int64_t total_tokens,
+                                  maxsim_dtype dtype, float *out, int32_t *argmax_out,
+                                  void *stream);
+
+/*
+ * maxsim_score_pq -- fused product-quantisation scoring (TileMaxSim §2(3)):
+ * the per-query table T[i,m,k] = q_i[m*(d/M) .. (m+1)*(d/M)) . C[m,k,:] is
+ * built once into the workspace, then each token's similarity is
+ * sum_m T[i, m, codes[j,m]] by table lookup; decoded vectors never exist.
+ *
+ *   Q          [nq, d] fp32
+ *   codebooks  [M, K, d/M] fp32 (d % M == 0, K <= 256)
+ *   codes      [total_tokens, M] uint8, CSR documents as in maxsim_score_varlen
+ *   out        [B] fp32; argmax_out [B, nq] int32 or NULL
+ *   workspace  >= maxsim_score_pq_workspace_size(nq, M, K) bytes, 256-byte aligned
+ *
+ * Limits: 1 <= nq <= 1024, 1 <= M <= 64, 1 <= K <= 256, d % M == 0, d <= 1024.
+ */
+size_t maxsim_score_pq_workspace_size(int nq, int M, int K);
+maxsim_status maxsim_score_pq(const float *Q, int nq, int d,
+                              const float *codebooks, int M, int K,
+                              const uint8_t *codes, const int64_t *offsets,
+                              int64_t B, int64_t total_tokens,
+                              float *out, int32_t *argmax_out,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * maxsim_score_i8 -- INT8 x INT8 scoring (FLASH-MAXSIM, Abstract) with
+ * per-token symmetric scales:
+ *   dot(i,j) = sum_k Q[i,k] * D[j,k]        exact int32
+ *   sim(i,j) = (float)dot(i,j) * d_scale[j] one fp32 multiply
+ *   m_i      = max_j sim(i,j)
+ *   out[b]   = sum_i q_scale[i] * m_i       fp32
+ *
+ *   Q [nq, d] int8, q_scale [nq] fp32 (> 0)
+ *   D [total_tokens, d] int8, d_scale [total_tokens] fp32 (> 0); CSR as above
+ *   out [B] fp32; maxv_out [B, nq] fp32 (m_i), maxdot_out [B, nq] int32
+ *   (dot at the argmax), argmax_out [B, nq] int32 -- each of the last three
+ *   may be NULL.
+ *
+ * Limits: 1 <= nq <= 256, d % 64 == 0, 64 <= d <= 1024 (|dot| < 2^24).
+ */
+maxsim_status maxsim_score_i8(const int8_t *Q, const float *q_scale, int nq, int d,
+                              const int8_t *D, const float *d_scale,
+                              const int64_t *offsets, int64_t B, int64_t total_tokens,
+                              float *out, float *maxv_out, int32_t *maxdot_out,
+                              int32_t *argmax_out, void *stream);
+
+/*
+ * maxsim_backward -- gradients through the forward argmax (FLASH-MAXSIM,
+ * Abstract: the backward pass reuses the forward argmax, with an
+ * inverse-grid CSR construction and an atomic-free, destination-owned
+ * gradient reduction). With loss = sum_{q,b} dS[q,b] * score[q,b] and
+ * a = argmax[q,b,i]:
+ *   dQ[q,i,:] = sum_b dS[q,b] * D[b, a, :]
+ *   dD[b,j,:] = sum_q dS[q,b] * sum_{i : a = j} Q[q,i,:]
+ * Each output row is written by exactly one thread block (no atomics); for
+ * dD every document's argmax entries are grouped by token (a counting sort
+ * on chip: the inverse CSR) before the sums.
+ *
+ *   Q [n_queries, nq, d], D [B, nd, d] (dtype BF16 or FP16), doc_len as in
+ *   maxsim_score; argmax [n_queries, B, nq] int32 from maxsim_score
+ *   (-1 = empty document); dS [n_queries, B] fp32.
+ *   dQ [n_queries, nq, d] fp32 and dD [B, nd, d] fp32 are fully written
+ *   (rows no argmax points at are 0).
+ *   workspace >= maxsim_backward_workspace_size(...) bytes (may be 0 -> NULL ok).
+ *
+ * Limits: d % 64 == 0, d <= 1024; n_queries * nq <= 65536; nd <= 65535.
+ * An argmax entry outside [-1, L_b) is skipped and sets MAXSIM_DEVERR_BAD_INPUT.
+ */
+size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd);
+maxsim_status maxsim_backward(const void *Q, int n_queries, int nq, int d,
+                              const void *D, int64_t B, int nd, const int32_t *doc_len,
+                              maxsim_dtype dtype, const int32_t *argmax, const float *dS,
+                              float *dQ, float *dD,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAXSIM_H_ */

@@ -1,0 +1,217 @@
+// api.cu -- the extern "C" entry points of libmaxsim.so (include/maxsim.h):
+// host-side argument validation, per-device facts, TMA descriptor encoding
+// and the device status word. All arithmetic of the operator lives in the
+// kernel translation units.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+
+namespace msim {
+
+// Per-device status word written by kernels (timeouts, bad documents).
+__device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo info;
+    if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return nullptr;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
+    info.status = static_cast<unsigned*>(addr);
+    if (cudaMemset(info.status, 0, sizeof(unsigned)) != cudaSuccess) return nullptr;
+    g_dev[dev] = info;
+    g_dev_ready[dev] = true;
+  }
+  return &g_dev[dev];
+}
+
+bool encode_tmap(void* tmap, int dtype_code, int rank, void* gaddr, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle128) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (!g_encode) return false;
+  CUtensorMapDataType dt;
+  switch (dtype_code) {
+    case 0: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
+    case 1: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+    case 2: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
+    default: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
+  }
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap), dt, static_cast<cuuint32_t>(rank), gaddr, gd, gs, bx,
+                              es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace msim
+
+using namespace msim;
+
+extern "C" {
+
+int maxsim_version(void) { return 100; }
+
+const char* maxsim_status_string(maxsim_status status) {
+  switch (status) {
+    case MAXSIM_OK: return "MAXSIM_OK";
+    case MAXSIM_ERR_INVALID_ARG: return "MAXSIM_ERR_INVALID_ARG: invalid argument";
+    case MAXSIM_ERR_UNSUPPORTED: return "MAXSIM_ERR_UNSUPPORTED: shape or dtype not supported";
+    case MAXSIM_ERR_CUDA: return "MAXSIM_ERR_CUDA: CUDA runtime or launch failure";
+    case MAXSIM_ERR_TIMEOUT: return "MAXSIM_ERR_TIMEOUT: a device pipeline wait timed out";
+    case MAXSIM_ERR_WORKSPACE: return "MAXSIM_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "MAXSIM_ERR_UNKNOWN";
+}
+
+maxsim_status maxsim_device_status(void* stream, unsigned int* flags) {
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MAXSIM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned h = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MAXSIM_ERR_CUDA;
+  if (cudaMemcpyAsync(&h, dev->status, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MAXSIM_ERR_CUDA;
+  if (cudaMemsetAsync(dev->status, 0, sizeof(unsigned), s) != cudaSuccess) return MAXSIM_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MAXSIM_ERR_CUDA;
+  if (flags) *flags = h;
+  if (h & MAXSIM_DEVERR_TIMEOUT) return MAXSIM_ERR_TIMEOUT;
+  if (h & MAXSIM_DEVERR_BAD_INPUT) return MAXSIM_ERR_INVALID_ARG;
+  return MAXSIM_OK;
+}
+
+static maxsim_status check_common(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B,
+                                  maxsim_dtype dtype, const float* out, const int32_t* argmax_out) {
+  if (n_queries < 1 || nq < 1 || d < 1 || B < 0) return MAXSIM_ERR_INVALID_ARG;
+  if (dtype != MAXSIM_BF16 && dtype != MAXSIM_FP16 && dtype != MAXSIM_FP32) return MAXSIM_ERR_INVALID_ARG;
+  if (!Q) return MAXSIM_ERR_INVALID_ARG;
+  if (B == 0) return MAXSIM_OK;  // nothing to score: D and out may be empty (NULL) buffers
+  if (!D || !out) return MAXSIM_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(D) || !aligned4(out) || (argmax_out && !aligned4(argmax_out)))
+    return MAXSIM_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_queries) * nq > INT_MAX / 2) return MAXSIM_ERR_UNSUPPORTED;
+  if (dtype == MAXSIM_FP32) {
+    if (d % 4 != 0 || d > 1024) return MAXSIM_ERR_UNSUPPORTED;
+  } else {
+    if (d % 64 != 0 || d > 1024) return MAXSIM_ERR_UNSUPPORTED;
+  }
+  return MAXSIM_OK;
+}
+
+maxsim_status maxsim_score(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                           const int32_t* doc_len, maxsim_dtype dtype, float* out, int32_t* argmax_out,
+                           void* stream) {
+  maxsim_status st = check_common(Q, n_queries, nq, d, D, B, dtype, out, argmax_out);
+  if (st != MAXSIM_OK) return st;
+  if (nd < 1 || (doc_len && !aligned4(doc_len))) return MAXSIM_ERR_INVALID_ARG;
+  if (B == 0) return MAXSIM_OK;
+  if (B > INT64_MAX / nd) return MAXSIM_ERR_INVALID_ARG;
+  const int64_t rows = B * static_cast<int64_t>(nd);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == MAXSIM_FP32)
+    return launch_fwd_f32(static_cast<const float*>(Q), n_queries, nq, d, static_cast<const float*>(D), rows, 0,
+                          doc_len, nullptr, B, nd, out, argmax_out, s);
+  return launch_fwd_tc(Q, n_queries, nq, d, D, rows, 0, doc_len, nullptr, B, nd, dtype == MAXSIM_BF16 ? 1 : 0, out,
+                       argmax_out, s);
+}
+
+maxsim_status maxsim_score_varlen(const void* Q, int n_queries, int nq, int d, const void* D_packed,
+                                  const int64_t* offsets, int64_t B, int64_t total_tokens, maxsim_dtype dtype,
+                                  float* out, int32_t* argmax_out, void* stream) {
+  if (!offsets || !aligned4(offsets) || total_tokens < 0) return MAXSIM_ERR_INVALID_ARG;
+  // No packed rows at all: D_packed may be an empty (NULL) buffer. It is never
+  // read; Q (same dtype, aligned) stands in so the descriptors can be encoded.
+  if (total_tokens == 0 && !D_packed) D_packed = Q;
+  maxsim_status st = check_common(Q, n_queries, nq, d, D_packed, B, dtype, out, argmax_out);
+  if (st != MAXSIM_OK) return st;
+  if (B == 0) return MAXSIM_OK;
+  // With total_tokens == 0 every document is empty: the kernels still run to
+  // write score 0 / argmax -1, and never read D_packed.
+  const int64_t rows = total_tokens > 0 ? total_tokens : 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == MAXSIM_FP32)
+    return launch_fwd_f32(static_cast<const float*>(Q), n_queries, nq, d, static_cast<const float*>(D_packed),
+                          total_tokens, 1, nullptr, offsets, B, 0, out, argmax_out, s);
+  return launch_fwd_tc(Q, n_queries, nq, d, D_packed, rows, 1, nullptr, offsets, B, 0,
+                       dtype == MAXSIM_BF16 ? 1 : 0, out, argmax_out, s);
+}
+
+size_t maxsim_score_pq_workspace_size(int nq, int M, int K) {
+  if (nq < 1 || M < 1 || K < 1) return 0;
+  return static_cast<size_t>(nq) * M * K * sizeof(float);
+}
+
+maxsim_status maxsim_score_pq(const float* Q, int nq, int d, const float* codebooks, int M, int K,
+                              const uint8_t* codes, const int64_t* offsets, int64_t B, int64_t total_tokens,
+                              float* out, int32_t* argmax_out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  (void)Q; (void)nq; (void)d; (void)codebooks; (void)M; (void)K; (void)codes; (void)offsets; (void)B;
+  (void)total_tokens; (void)out; (void)argmax_out; (void)workspace; (void)workspace_bytes; (void)stream;
+  return MAXSIM_ERR_UNSUPPORTED;
+}
+
+maxsim_status maxsim_score_i8(const int8_t* Q, const float* q_scale, int nq, int d, const int8_t* D,
+                              const float* d_scale, const int64_t* offsets, int64_t B, int64_t total_tokens,
+                              float* out, float* maxv_out, int32_t* maxdot_out, int32_t* argmax_out,
+                              void* stream) {
+  (void)Q; (void)q_scale; (void)nq; (void)d; (void)D; (void)d_scale; (void)offsets; (void)B; (void)total_tokens;
+  (void)out; (void)maxv_out; (void)maxdot_out; (void)argmax_out; (void)stream;
+  return MAXSIM_ERR_UNSUPPORTED;
+}
+
+size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd) {
+  (void)n_queries; (void)nq; (void)d; (void)B; (void)nd;
+  return 0;
+}
+
+maxsim_status maxsim_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                              const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
+                              float* dQ, float* dD, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)Q; (void)n_queries; (void)nq; (void)d; (void)D; (void)B; (void)nd; (void)doc_len; (void)dtype;
+  (void)argmax; (void)dS; (void)dQ; (void)dD; (void)workspace; (void)workspace_bytes; (void)stream;
+  return MAXSIM_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

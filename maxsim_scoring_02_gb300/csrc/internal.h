@@ -1,0 +1,40 @@
+// internal.h -- declarations shared between the kernel translation units and
+// the C-ABI layer. Not installed; the public interface is include/maxsim.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/maxsim.h"
+
+namespace msim {
+
+// Per-device facts the launchers need (cached by the C-ABI layer).
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;
+  unsigned* status;  // device address of the per-device status word
+};
+
+// Returns nullptr if the device could not be queried.
+const DeviceInfo* device_info();
+
+// Forward scoring on tcgen05 tensor cores (bf16 / fp16 inputs).
+// Documents are given either padded (csr = 0: rows b*nd .. b*nd+L_b-1, L_b
+// from doc_len or nd) or CSR (csr = 1: rows offsets[b] .. offsets[b+1]-1).
+maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const void* D, int64_t total_rows,
+                            int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
+                            int is_bf16, float* out, int32_t* argmax, cudaStream_t stream);
+
+// Forward scoring with fp32 inputs on the CUDA cores (FFMA).
+maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const float* D, int64_t total_rows,
+                             int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
+                             float* out, int32_t* argmax, cudaStream_t stream);
+
+// Encodes a TMA tensor map through the driver entry point (no libcuda link).
+// Returns false if the driver call is unavailable or rejects the arguments.
+bool encode_tmap(void* tmap, int dtype_code, int rank, void* gaddr, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle128);
+
+}  // namespace msim
