@@ -6,33 +6,39 @@
 // (TileMaxSim deep reading §1; FLASH-MAXSIM Figure 1 / Algorithm 2).
 //
 // Design (GB300 / sm_103a):
-//  * Persistent grid, one CTA per SM; CTA c owns a contiguous document range,
-//    so it streams one contiguous slab of D and every document byte is read
-//    from HBM exactly once per (query, query-chunk) -- with one query of up
-//    to 256 tokens that is the single pass of TileMaxSim §2(1) (BQ = Nq).
-//  * Warp 4 (one lane) is the TMA producer: 128-token x 64-dim boxes,
-//    128-byte swizzled, into a ring of 16 KB stages. Partial tiles (the tail
-//    of a document) load only ceil(rows/32)*32 rows, so padding beyond that
-//    granule is never read (TileMaxSim §5, the padding waste).
-//  * Warp 5 (one lane) issues tcgen05.mma kind::f16, M = 128 document tokens,
-//    N = NC query tokens, K = 16 per instruction, accumulating every 64-wide
-//    d-slice of the tile into the same TMEM accumulator before any maximum is
-//    taken (TileMaxSim §2(2), dimension tiling). Several TMEM accumulators
-//    let the tensor core run ahead of the epilogue.
-//  * Warps 0-3 read the accumulator (TMEM lane = document token, column =
-//    query token) with tcgen05.ld, mask tokens outside the document to -inf,
-//    and reduce the 32 rows a warp holds with a transpose butterfly of
-//    shuffles, leaving lane l with the maximum (and lowest argmax) of query
-//    column l. Per-warp partial maxima persist across the document's tiles in
-//    registers; at the document end the four warps combine through shared
-//    memory and the per-token maxima are summed. The Nq x Nd similarity tile
-//    exists only in TMEM and registers.
-//  * Every mbarrier wait is bounded (see ptx.cuh); after an abort the
-//    producer drains its in-flight TMA loads and the MMA warp waits for its
-//    last MMA before TMEM is released.
+//  * Documents are cut into 32-row chunks. A 128-row MMA tile holds four
+//    chunk slots; slot w is TMEM lanes 32w..32w+31 and is reduced by epilogue
+//    warp w, so a warp's 32 rows always belong to ONE document. Short
+//    documents therefore share tiles (four 32-token documents per tile), long
+//    ones span tiles, and padding beyond a document's last 32-row granule is
+//    never loaded (TileMaxSim §5, the padding waste). Padded (length-masked)
+//    and CSR layouts only differ in where a document's rows start.
+//  * Persistent grid, one CTA per SM; CTA c owns a contiguous document range
+//    and walks it in groups of up to 256 chunks. The producer warp builds each
+//    group's slot table in shared memory (32 lanes load the document offsets
+//    in parallel), so no role waits on a global load in its issue loop.
+//  * Producer (warp 4, lane 0 issues): TMA loads of 64-dim x 32/128-row boxes,
+//    128-byte swizzled, into a ring of 16 KB stages; four contiguous slots go
+//    as one 128-row box. Every document byte is read from HBM once per
+//    (query, query chunk) pass -- with one query of up to 256 tokens that is
+//    the single pass of TileMaxSim §2(1) (BQ = Nq). With several queries or
+//    query chunks, all passes run over one group (<= 256 chunks) before the
+//    next, so the repeats are served by L2.
+//  * MMA (warp 5, lane 0 issues): tcgen05.mma kind::f16, M = 128 rows, N = NC
+//    query tokens, K = 16; every 64-wide d-slice of a tile accumulates into
+//    the same TMEM accumulator before any maximum is taken (TileMaxSim §2(2),
+//    dimension tiling). Up to four accumulators let it run ahead.
+//  * Epilogue (warps 0-3): tcgen05.ld of the warp's 32 lanes, rows past the
+//    chunk's valid rows masked to -inf, a transpose butterfly of shuffles
+//    leaves lane l with the maximum (and lowest argmax) of query column l
+//    over the slot; slot partials are merged in document order through shared
+//    memory and each finished document's maxima are summed (FLASH-MAXSIM
+//    Figure 1: only the scalar score is written). The similarity tile exists
+//    only in TMEM and registers.
+//  * Every mbarrier wait is bounded (ptx.cuh); after an abort the producer
+//    drains its in-flight TMA loads and the MMA thread waits for its last MMA
+//    before TMEM is released.
 #include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -46,9 +52,11 @@ namespace {
 
 constexpr int kThreads = 192;        // warps 0-3 epilogue, 4 producer, 5 MMA
 constexpr int kStageBytes = 16384;   // 128 rows x 64 elements x 2 bytes
-constexpr int kTileRows = 128;
-constexpr int kRowGranule = 32;      // rows per TMA box for partial tiles
+constexpr int kSlotRows = 32;
+constexpr int kCapSlots = 256;       // chunk slots per group table
+constexpr int kCapDocs = 256;        // documents per group table
 constexpr int kMaxAcc = 4;
+constexpr int kMaxFin = 5;           // documents finished per tile (4 slots + pass end)
 
 struct FwdTcParams {
   const int32_t* doc_len;   // padded layout, may be null
@@ -61,6 +69,7 @@ struct FwdTcParams {
   int nq;
   int KB;          // d / 64
   int n_chunks;    // ceil(nq / NC)
+  int multipass;   // n_queries * n_chunks > 1
   int stages;
   int n_acc;
   int n_qslots;
@@ -71,13 +80,85 @@ struct FwdTcParams {
   unsigned* status;
 };
 
-// Rows of document b: returns L_b and sets start; a document whose
-// description is out of range is reported as bad and treated as empty.
+// One group of documents, written by the producer warp, read by all roles.
+struct GroupTab {
+  int32_t n_docs;          // documents in the group (incl. empty ones); -1 = end of work
+  int32_t n_slots;         // chunk slots used
+  int64_t first_doc;       // global index of local document 0
+  int32_t slot_row[kCapSlots];   // first row of the chunk in D
+  int32_t slot_info[kCapSlots];  // (chunk index in doc << 6) | valid rows (1..32)
+  int32_t slot_doc[kCapSlots];   // local document index
+  int32_t doc_len[kCapDocs];     // 0 for empty (or rejected) documents
+};
+
+struct Smem {
+  uint8_t* q;            // n_qslots x KB boxes of NC rows x 128 B
+  uint8_t* stages;       // stages x 16 KB
+  GroupTab* tab;         // [2]
+  uint64_t* bars;        // full[S] empty[S] qfull[2] qempty[2] accfull[A] accempty[A] tabfull[2] tabempty[2] done
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+  float* part_v;         // [2][4][NC]
+  int32_t* part_i;       // [2][4][NC]
+  float* psum;           // [2][4][kMaxFin]
+  float* gsum;           // [kCapDocs]
+};
+
+__host__ __device__ inline size_t bars_count(int stages, int n_acc) { return 2 * stages + 4 + 2 * n_acc + 4 + 1; }
+
+__host__ __device__ inline size_t smem_bytes_for(int NC, int KB, int stages, int n_acc, int n_qslots) {
+  size_t bytes = 1024;  // alignment slack for the dynamic region
+  bytes += static_cast<size_t>(n_qslots) * KB * NC * 128;
+  bytes += static_cast<size_t>(stages) * kStageBytes;
+  bytes += 2 * sizeof(GroupTab);
+  bytes += bars_count(stages, n_acc) * 8;
+  bytes += 16;
+  bytes += static_cast<size_t>(2 * 4 * NC) * 8;
+  bytes += 2 * 4 * kMaxFin * 4;
+  bytes += kCapDocs * 4;
+  return bytes;
+}
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, const FwdTcParams& p, int NC) {
+  Smem s;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.q = base;
+  s.stages = s.q + static_cast<size_t>(p.n_qslots) * p.KB * NC * 128;
+  s.tab = reinterpret_cast<GroupTab*>(s.stages + static_cast<size_t>(p.stages) * kStageBytes);
+  s.bars = reinterpret_cast<uint64_t*>(s.tab + 2);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + bars_count(p.stages, p.n_acc));
+  s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  s.part_v = reinterpret_cast<float*>(s.tmem_slot + 4);
+  s.part_i = reinterpret_cast<int32_t*>(s.part_v + 2 * 4 * NC);
+  s.psum = reinterpret_cast<float*>(s.part_i + 2 * 4 * NC);
+  s.gsum = s.psum + 2 * 4 * kMaxFin;
+  return s;
+}
+
+// Barrier addresses (32-bit shared) in the order laid out by carve().
+struct Bars {
+  uint32_t full, empty, qfull, qempty, accfull, accempty, tabfull, tabempty, done;
+  __device__ __forceinline__ Bars(const Smem& sm, int S, int A) {
+    const uint32_t b0 = smem_u32(sm.bars);
+    full = b0;
+    empty = full + 8 * S;
+    qfull = empty + 8 * S;
+    qempty = qfull + 16;
+    accfull = qempty + 16;
+    accempty = accfull + 8 * A;
+    tabfull = accempty + 8 * A;
+    tabempty = tabfull + 16;
+    done = tabempty + 16;
+  }
+};
+
+// Rows of document b (start row and length); out-of-range descriptions are
+// reported as bad and scored as empty documents.
 __device__ __forceinline__ int64_t doc_rows(const FwdTcParams& p, int64_t b, int64_t& start, bool& bad) {
   bad = false;
   if (p.csr) {
     const int64_t s = __ldg(p.offsets + b), e = __ldg(p.offsets + b + 1);
-    if (s < 0 || e < s || e > p.total_rows || e - s > INT_MAX) {
+    if (s < 0 || e < s || e > p.total_rows) {
       bad = true;
       start = 0;
       return 0;
@@ -94,168 +175,260 @@ __device__ __forceinline__ int64_t doc_rows(const FwdTcParams& p, int64_t b, int
   return L;
 }
 
-struct Smem {
-  uint8_t* q;         // n_qslots x KB boxes of NC rows x 128 B
-  uint8_t* stages;    // stages x 16 KB
-  uint64_t* full;
-  uint64_t* empty;
-  uint64_t* qfull;    // [2]
-  uint64_t* qempty;   // [2]
-  uint64_t* accfull;  // [n_acc]
-  uint64_t* accempty; // [n_acc]
-  uint64_t* done;
-  uint32_t* tmem_slot;
-  volatile int* abort_flag;
-  float* red_v;       // [2][4][NC]
-  int32_t* red_i;     // [2][4][NC]
-  float* sred;        // [2][4]
-};
-
-__host__ __device__ inline size_t smem_bytes_for(int NC, int KB, int stages, int n_acc, int n_qslots) {
-  size_t bytes = 1024;  // alignment slack for the dynamic region
-  bytes += static_cast<size_t>(n_qslots) * KB * NC * 128;
-  bytes += static_cast<size_t>(stages) * kStageBytes;
-  bytes += static_cast<size_t>(2 * stages + 4 + 2 * n_acc + 1) * 8;
-  bytes += 16;  // tmem slot + abort flag (+pad)
-  bytes += static_cast<size_t>(2 * 4 * NC) * 8;  // red_v + red_i
-  bytes += 2 * 4 * 4;
-  return bytes;
-}
-
-__device__ __forceinline__ Smem carve(uint8_t* raw, const FwdTcParams& p, int NC) {
-  Smem s;
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-  s.q = base;
-  s.stages = s.q + static_cast<size_t>(p.n_qslots) * p.KB * NC * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.stages + static_cast<size_t>(p.stages) * kStageBytes);
-  s.full = bars;
-  s.empty = s.full + p.stages;
-  s.qfull = s.empty + p.stages;
-  s.qempty = s.qfull + 2;
-  s.accfull = s.qempty + 2;
-  s.accempty = s.accfull + p.n_acc;
-  s.done = s.accempty + p.n_acc;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.done + 1);
-  s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
-  s.red_v = reinterpret_cast<float*>(s.tmem_slot + 4);
-  s.red_i = reinterpret_cast<int32_t*>(s.red_v + 2 * 4 * NC);
-  s.sred = reinterpret_cast<float*>(s.red_i + 2 * 4 * NC);
-  return s;
-}
-
 // ------------------------------------------------------------ producer warp
+// Builds the slot table of the next group (all 32 lanes). `nb` / `carry` is
+// the walk position: next document and, in single-pass mode, the number of
+// its chunks already placed in earlier groups (a long document may be split
+// across groups there; in multi-pass mode a group always holds whole
+// documents).
+__device__ void build_group(const FwdTcParams& p, GroupTab* T, int64_t& nb, int64_t b1, int64_t& carry) {
+  const int lane = threadIdx.x & 31;
+  int nslots = 0, ndocs = 0;
+  if (lane == 0) T->first_doc = nb;
+  const int64_t carry0 = carry;
+  while (nb < b1 && ndocs < kCapDocs && nslots < kCapSlots) {
+    const int64_t b = nb + lane;
+    const bool in = b < b1 && ndocs + lane < kCapDocs;
+    int64_t start = 0, L = 0;
+    bool bad = false;
+    if (in) L = doc_rows(p, b, start, bad);
+    if (bad) atomicOr(p.status, kDevErrBadInput);
+    const int64_t ck0 = (lane == 0) ? carry : 0;   // chunks of this doc already placed
+    int64_t chunks = in ? (L + kSlotRows - 1) / kSlotRows - ck0 : 0;
+    if (p.multipass && chunks > kCapSlots) {        // cannot fit a group: reject
+      atomicOr(p.status, kDevErrBadInput);
+      chunks = 0;
+      L = 0;
+    }
+    // inclusive scan of chunk counts (saturated to the capacity)
+    int c32 = static_cast<int>(chunks > kCapSlots ? kCapSlots + 1 : chunks);
+    int incl = c32;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl = min(incl + v, 1 << 20);
+    }
+    const int pre = incl - c32;
+    const int room = kCapSlots - nslots;
+    // a lane's document is accepted whole if it fits; in single-pass mode the
+    // first one that does not fit is placed partially (split)
+    const bool whole = in && (pre + c32 <= room);
+    const unsigned acc_mask = __ballot_sync(0xffffffffu, whole);
+    const int n_whole = __popc(~acc_mask) == 0 ? 32 : __ffs(~acc_mask) - 1;  // accepted lanes form a prefix
+    bool split = false;
+    int placed = whole ? c32 : 0;
+    if (!p.multipass && lane == n_whole && in && pre < room) {
+      split = true;
+      placed = room - pre;
+    }
+    const unsigned split_mask = __ballot_sync(0xffffffffu, split);
+    if (whole || split) {
+      const int dl = ndocs + lane;
+      T->doc_len[dl] = static_cast<int32_t>(L);
+      for (int k = 0; k < placed; ++k) {
+        const int idx = nslots + pre + k;
+        const int64_t ck = ck0 + k;
+        const int64_t rowk = start + ck * kSlotRows;
+        const int64_t left = L - ck * kSlotRows;
+        T->slot_row[idx] = static_cast<int32_t>(rowk);
+        T->slot_info[idx] = static_cast<int32_t>((ck << 6) | (left >= kSlotRows ? kSlotRows : left));
+        T->slot_doc[idx] = dl;
+      }
+    }
+    // totals (from the last placing lane)
+    const int last = split_mask ? (__ffs(split_mask) - 1) : (n_whole - 1);
+    int tot = 0;
+    if (last >= 0) tot = __shfl_sync(0xffffffffu, pre + placed, last);
+    int split_placed = split_mask ? __shfl_sync(0xffffffffu, placed, __ffs(split_mask) - 1) : 0;
+    nslots += tot;
+    ndocs += n_whole + (split_mask ? 1 : 0);
+    if (split_mask) {
+      carry = (n_whole == 0 ? carry : 0) + split_placed;
+      nb += n_whole;
+      break;
+    }
+    if (n_whole > 0) carry = 0;
+    nb += n_whole;
+    if (n_whole < 32) break;   // capacity reached (docs or slots)
+  }
+  (void)carry0;
+  if (lane == 0) {
+    T->n_docs = ndocs;
+    T->n_slots = nslots;
+  }
+  __syncwarp();
+}
+
 template <int NC>
-__device__ void run_producer(const FwdTcParams& p, const Smem& sm, const CUtensorMap* tm_d128,
+__device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& br, const CUtensorMap* tm_d128,
                              const CUtensorMap* tm_d32, const CUtensorMap* tm_q, int64_t b0, int64_t b1) {
+  const int lane = threadIdx.x & 31;
   const int S = p.stages, KB = p.KB, NQS = p.n_qslots;
   const uint32_t qbytes = static_cast<uint32_t>(KB) * NC * 128;
   const uint64_t policy = l2_policy_evict_first();
-  uint32_t fill = 0, quse = 0;
+  const uint32_t stage0 = smem_u32(sm.stages);
+  const uint32_t q0 = smem_u32(sm.q);
+  int s = 0;
+  uint32_t ph = 0, fills = 0, quse = 0;
   int prev_key = -1;
-  for (int64_t b = b0; b < b1; ++b) {
-    int64_t start;
-    bool bad;
-    const int64_t L = doc_rows(p, b, start, bad);
-    if (L == 0) continue;
-    const int ntiles = static_cast<int>((L + kTileRows - 1) / kTileRows);
-    for (int q = 0; q < p.n_queries; ++q) {
-      for (int c = 0; c < p.n_chunks; ++c) {
-        const int key = q * p.n_chunks + c;
-        if (key != prev_key) {
-          const int slot = static_cast<int>(quse % NQS);
-          const uint32_t use = quse / NQS;
-          if (use > 0 && !mbar_wait(&sm.qempty[slot], (use - 1) & 1u, sm.abort_flag, p.status)) goto drain;
-          mbar_arrive_expect_tx(&sm.qfull[slot], qbytes);
-          for (int kb = 0; kb < KB; ++kb)
-            tma_load_3d(sm.q + (static_cast<size_t>(slot) * KB + kb) * NC * 128, tm_q, &sm.qfull[slot], kb * 64,
-                        c * NC, q);
-          ++quse;
-          prev_key = key;
-        }
-        for (int t = 0; t < ntiles; ++t) {
-          const int64_t row0 = start + static_cast<int64_t>(t) * kTileRows;
-          const int64_t left = L - static_cast<int64_t>(t) * kTileRows;
-          const int rows = left >= kTileRows ? kTileRows : static_cast<int>(left);
-          const int rows_ld = rows == kTileRows ? kTileRows : ((rows + kRowGranule - 1) / kRowGranule) * kRowGranule;
-          for (int kb = 0; kb < KB; ++kb) {
-            const int s = static_cast<int>(fill % S);
-            const uint32_t ph = (fill / S) & 1u;
-            if (!mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status)) goto drain;
-            mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(rows_ld) * 128u);
-            uint8_t* dst = sm.stages + static_cast<size_t>(s) * kStageBytes;
-            if (rows_ld == kTileRows) {
-              tma_load_2d_hint(dst, tm_d128, &sm.full[s], kb * 64, static_cast<int>(row0), policy);
-            } else {
-              for (int r = 0; r < rows_ld; r += kRowGranule)
-                tma_load_2d_hint(dst + r * 128, tm_d32, &sm.full[s], kb * 64, static_cast<int>(row0 + r), policy);
+  int64_t nb = b0, carry = 0;
+  bool ok = true;
+  for (uint32_t gi = 0; ok; ++gi) {
+    const int buf = gi & 1;
+    GroupTab* T = sm.tab + buf;
+    if (gi >= 2) {
+      bool w = true;
+      if (lane == 0) w = mbar_wait_a(br.tabempty + 8 * buf, ((gi >> 1) - 1) & 1u, sm.abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) { ok = false; break; }
+    }
+    const bool end = nb >= b1;
+    if (end) {
+      if (lane == 0) T->n_docs = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
+      break;
+    }
+    build_group(p, T, nb, b1, carry);
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
+    if (lane == 0) {
+      const int n_slots = T->n_slots;
+      const int n_tiles = (n_slots + 3) >> 2;
+      for (int q = 0; q < p.n_queries && ok; ++q) {
+        for (int c = 0; c < p.n_chunks && ok; ++c) {
+          if (n_tiles == 0) continue;
+          const int key = q * p.n_chunks + c;
+          if (key != prev_key) {
+            const int slot = static_cast<int>(quse % NQS);
+            const uint32_t use = quse / NQS;
+            if (use > 0 && !mbar_wait_a(br.qempty + 8 * slot, (use - 1) & 1u, sm.abort_flag, p.status)) {
+              ok = false;
+              break;
             }
-            ++fill;
+            mbar_arrive_expect_tx_a(br.qfull + 8 * slot, qbytes);
+            for (int kb = 0; kb < KB; ++kb)
+              tma_load_3d_a(q0 + static_cast<uint32_t>((slot * KB + kb) * NC * 128), tm_q, br.qfull + 8 * slot,
+                            kb * 64, c * NC, q);
+            ++quse;
+            prev_key = key;
+          }
+          for (int t = 0; t < n_tiles && ok; ++t) {
+            const int i0 = 4 * t;
+            const int nslot = min(4, n_slots - i0);
+            int rows[4];
+            bool contiguous = nslot == 4;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              rows[w] = w < nslot ? T->slot_row[i0 + w] : 0;
+              if (w > 0 && rows[w] != rows[0] + 32 * w) contiguous = false;
+            }
+            const uint32_t bytes = contiguous ? 16384u : static_cast<uint32_t>(nslot) * 4096u;
+            for (int kb = 0; kb < KB; ++kb) {
+              if (!mbar_wait_a(br.empty + 8 * s, ph ^ 1u, sm.abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb = br.full + 8 * s;
+              const uint32_t dst = stage0 + static_cast<uint32_t>(s) * kStageBytes;
+              mbar_arrive_expect_tx_a(fb, bytes);
+              if (contiguous) {
+                tma_load_2d_a(dst, tm_d128, fb, kb * 64, rows[0], policy);
+              } else {
+                for (int w = 0; w < nslot; ++w) tma_load_2d_a(dst + w * 4096u, tm_d32, fb, kb * 64, rows[w], policy);
+              }
+              ++fills;
+              if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+              }
+            }
           }
         }
       }
     }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   }
-  return;
-drain:
-  // After an abort: wait (bounded) for every load this warp may still have in flight.
-  for (uint32_t f = fill > static_cast<uint32_t>(S) ? fill - S : 0; f < fill; ++f)
-    mbar_wait_drain(&sm.full[f % S], (f / S) & 1u, p.status);
-  for (uint32_t u = quse > static_cast<uint32_t>(NQS) ? quse - NQS : 0; u < quse; ++u)
-    mbar_wait_drain(&sm.qfull[u % NQS], (u / NQS) & 1u, p.status);
+  if (!ok && lane == 0) {
+    // After an abort: wait (bounded) for every load this warp may still have in flight.
+    for (uint32_t f = fills > static_cast<uint32_t>(S) ? fills - S : 0; f < fills; ++f)
+      mbar_wait_drain(sm.bars + (f % S), (f / S) & 1u, p.status);
+    for (uint32_t u = quse > static_cast<uint32_t>(NQS) ? quse - NQS : 0; u < quse; ++u)
+      mbar_wait_drain(sm.bars + 2 * S + (u % NQS), (u / NQS) & 1u, p.status);
+  }
 }
 
 // ----------------------------------------------------------------- MMA warp
 template <int NC>
-__device__ void run_mma(const FwdTcParams& p, const Smem& sm, uint32_t tmem_base, int64_t b0, int64_t b1) {
+__device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
   const int S = p.stages, KB = p.KB, NQS = p.n_qslots, A = p.n_acc;
-  uint32_t fill = 0, quse = 0, acc = 0;
+  const uint32_t idesc = p.idesc;
+  const uint64_t adesc0 = sdesc_k_sw128(smem_u32(sm.stages));
+  const uint64_t qdesc0 = sdesc_k_sw128(smem_u32(sm.q));
+  int s = 0, a = 0;
+  uint32_t ph = 0, aph = 0, quse = 0;
   int prev_key = -1, slot = 0;
-  for (int64_t b = b0; b < b1; ++b) {
-    int64_t start;
-    bool bad;
-    const int64_t L = doc_rows(p, b, start, bad);
-    if (L == 0) continue;
-    const int ntiles = static_cast<int>((L + kTileRows - 1) / kTileRows);
-    for (int q = 0; q < p.n_queries; ++q) {
-      for (int c = 0; c < p.n_chunks; ++c) {
+  for (uint32_t gi = 0;; ++gi) {
+    const int buf = gi & 1;
+    if (!mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) break;
+    const GroupTab* T = sm.tab + buf;
+    if (T->n_docs < 0) break;
+    const int n_tiles = (T->n_slots + 3) >> 2;
+    bool ok = true;
+    for (int q = 0; q < p.n_queries && ok; ++q) {
+      for (int c = 0; c < p.n_chunks && ok; ++c) {
+        if (n_tiles == 0) continue;
         const int key = q * p.n_chunks + c;
         if (key != prev_key) {
-          if (prev_key >= 0) umma_commit(&sm.qempty[slot]);  // slot free once its MMAs retire
+          if (prev_key >= 0) umma_commit_a(br.qempty + 8 * slot);  // slot free once its MMAs retire
           slot = static_cast<int>(quse % NQS);
-          if (!mbar_wait(&sm.qfull[slot], (quse / NQS) & 1u, sm.abort_flag, p.status)) goto drain;
+          if (!mbar_wait_a(br.qfull + 8 * slot, (quse / NQS) & 1u, sm.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           ++quse;
           prev_key = key;
         }
-        const uint32_t qbase = smem_u32(sm.q + static_cast<size_t>(slot) * KB * NC * 128);
-        for (int t = 0; t < ntiles; ++t) {
-          const int a = static_cast<int>(acc % A);
-          if (!mbar_wait(&sm.accempty[a], ((acc / A) & 1u) ^ 1u, sm.abort_flag, p.status)) goto drain;
+        const uint64_t qdesc = qdesc0 + static_cast<uint64_t>((slot * KB * NC * 128) >> 4);
+        for (int t = 0; t < n_tiles; ++t) {
+          if (!mbar_wait_a(br.accempty + 8 * a, aph ^ 1u, sm.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * NC);
           for (int kb = 0; kb < KB; ++kb) {
-            const int s = static_cast<int>(fill % S);
-            if (!mbar_wait(&sm.full[s], (fill / S) & 1u, sm.abort_flag, p.status)) goto drain;
+            if (!mbar_wait_a(br.full + 8 * s, ph, sm.abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(sm.stages + static_cast<size_t>(s) * kStageBytes);
-            const uint32_t b_addr = qbase + static_cast<uint32_t>(kb * NC * 128);
+            const uint64_t ad = adesc0 + static_cast<uint64_t>(s * (kStageBytes >> 4));
+            const uint64_t bd = qdesc + static_cast<uint64_t>((kb * NC * 128) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_f16(d_tmem, sdesc_k_sw128(a_addr + kk * 32), sdesc_k_sw128(b_addr + kk * 32), p.idesc,
-                       (kb | kk) != 0 ? 1u : 0u);
-            umma_commit(&sm.empty[s]);  // stage reusable once these MMAs have read it
-            ++fill;
+            for (int kk = 0; kk < 4; ++kk) umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_commit_a(br.empty + 8 * s);  // stage reusable once these MMAs have read it
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
-          umma_commit(&sm.accfull[a]);  // accumulator ready for the epilogue
-          ++acc;
+          if (!ok) break;
+          umma_commit_a(br.accfull + 8 * a);  // accumulator ready for the epilogue
+          if (++a == A) {
+            a = 0;
+            aph ^= 1u;
+          }
         }
       }
     }
+    if (!ok) break;
+    mbar_arrive_a(br.tabempty + 8 * buf);
   }
-drain:
   // Wait until every MMA issued by this thread has completed before TMEM is freed.
-  umma_commit(sm.done);
-  mbar_wait_drain(sm.done, 0, p.status);
+  umma_commit_a(br.done);
+  mbar_wait_drain(sm.bars + (br.done - br.full) / 8, 0, p.status);
 }
 
 // Max over the 32 lanes of a warp for each of 32 columns: on return lane l
@@ -290,115 +463,246 @@ __device__ __forceinline__ void warp_column_max(float (&v)[32], int row, int lan
   out_i = ix[0];
 }
 
+// Appends (doc, sum) to the finished-document list without dynamic indexing.
+__device__ __forceinline__ void fin_push(int64_t (&fd)[kMaxFin], float (&fs)[kMaxFin], int& n, int64_t doc,
+                                         float sum) {
+#pragma unroll
+  for (int f = 0; f < kMaxFin; ++f)
+    if (f == n) {
+      fd[f] = doc;
+      fs[f] = sum;
+    }
+  ++n;
+}
+
 // ------------------------------------------------------------ epilogue warps
 template <int NG, bool ARGMAX>
-__device__ void run_epilogue(const FwdTcParams& p, const Smem& sm, uint32_t tmem_base, int64_t b0, int64_t b1) {
+__device__ void run_epilogue(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
   constexpr int NC = 32 * NG;
-  const int tid = threadIdx.x;  // 0..127 == TMEM lane
+  constexpr int R = NC > 128 ? 2 : 1;   // merge columns per thread
+  const int tid = threadIdx.x;          // 0..127 == TMEM lane
   const int warp = tid >> 5, lane = tid & 31;
   const int A = p.n_acc;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  uint32_t acc = 0;
-  int rb = 0;
-  for (int64_t b = b0; b < b1; ++b) {
-    int64_t start;
-    bool bad;
-    const int64_t L = doc_rows(p, b, start, bad);
-    if (bad && tid == 0) atomicOr(p.status, kDevErrBadInput);
-    const int ntiles = static_cast<int>((L + kTileRows - 1) / kTileRows);
+  const bool has_col = tid < NC;
+  int a = 0, pb = 0;
+  uint32_t aph = 0;
+  // running state of the current document for this thread's merge columns
+  int64_t cur = -1;
+  float rm[R];
+  int ra[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    rm[r] = -INFINITY;
+    ra[r] = INT_MAX;
+  }
+  for (uint32_t gi = 0;; ++gi) {
+    const int buf = gi & 1;
+    if (!mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) return;
+    const GroupTab* T = sm.tab + buf;
+    const int n_docs = T->n_docs;
+    if (n_docs < 0) break;
+    const int n_slots = T->n_slots;
+    const int n_tiles = (n_slots + 3) >> 2;
+    const int64_t first = T->first_doc;
     for (int q = 0; q < p.n_queries; ++q) {
-      float qsum = 0.f;
       for (int c = 0; c < p.n_chunks; ++c) {
-        if (L == 0) {
-          if (ARGMAX)
-            for (int col = tid; col < NC; col += 128) {
-              const int qc = c * NC + col;
-              if (qc < p.nq) p.argmax[(static_cast<int64_t>(q) * p.B + b) * p.nq + qc] = -1;
-            }
-          continue;
+        const bool last_chunk = c == p.n_chunks - 1;
+        // empty documents of the group: score 0, argmax -1 (no slots, no MMA)
+        for (int dl = tid; dl < n_docs; dl += 128) {
+          if (T->doc_len[dl] == 0) {
+            const int64_t b = first + dl;
+            if (ARGMAX)
+              for (int col = 0; col < NC; ++col) {
+                const int qc = c * NC + col;
+                if (qc < p.nq) p.argmax[(static_cast<int64_t>(q) * p.B + b) * p.nq + qc] = -1;
+              }
+            if (last_chunk) p.out[static_cast<int64_t>(q) * p.B + b] = 0.f;
+          }
         }
-        float rm[NG];
-        int ra[NG];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          rm[g] = -INFINITY;
-          ra[g] = INT_MAX;
-        }
-        for (int t = 0; t < ntiles; ++t) {
-          const int a = static_cast<int>(acc % A);
-          if (!mbar_wait(&sm.accfull[a], (acc / A) & 1u, sm.abort_flag, p.status)) return;
+        if (p.multipass) cur = -1;
+        for (int t = 0; t < n_tiles; ++t) {
+          if (!mbar_wait_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
           tc_fence_after();
-          const int row = t * kTileRows + tid;
-          const bool valid = row < L;
+          const int i0 = 4 * t;
+          const int nslot = min(4, n_slots - i0);
+          float* pv = sm.part_v + pb * 4 * NC;
+          int32_t* pi = sm.part_i + pb * 4 * NC;
+          if (warp < nslot) {
+            const int info = T->slot_info[i0 + warp];
+            const int vrows = info & 63;
+            const int row = (info >> 6) * kSlotRows + lane;   // doc-local token index of this lane's row
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            float v[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(a * NC + g * 32), v);
-            if (!valid) {
+            for (int g = 0; g < NG; ++g) {
+              float v[32];
+              tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(a * NC + g * 32), v);
+              if (g == NG - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
+              }
+              if (lane >= vrows) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) v[k] = -INFINITY;
+                for (int k = 0; k < 32; ++k) v[k] = -INFINITY;
+              }
+              float bv;
+              int bi;
+              warp_column_max<ARGMAX>(v, row, lane, bv, bi);
+              pv[warp * NC + g * 32 + lane] = bv;
+              if (ARGMAX) pi[warp * NC + g * 32 + lane] = bi;
             }
-            float bv;
-            int bi;
-            warp_column_max<ARGMAX>(v, row, lane, bv, bi);
-            if (ARGMAX) {
-              if (bv > rm[g] || (bv == rm[g] && bi < ra[g])) {
-                rm[g] = bv;
-                ra[g] = bi;
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
+          }
+          if (++a == A) {
+            a = 0;
+            aph ^= 1u;
+          }
+          named_bar_sync(1, 128);
+          // merge the slot partials in document order; collect finished documents
+          int nfin = 0;
+          int64_t fin_doc[kMaxFin];
+          float fin_sum[kMaxFin];
+          const bool pass_end = p.multipass && (t == n_tiles - 1);
+          for (int w = 0; w < nslot; ++w) {
+            const int64_t dg = first + T->slot_doc[i0 + w];
+            if (dg != cur) {
+              if (cur >= 0) {
+                float sum = 0.f;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  const int col = tid + 128 * r;
+                  const int qc = c * NC + col;
+                  if (has_col && col < NC && qc < p.nq) {
+                    sum += rm[r];
+                    if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + cur) * p.nq + qc] = ra[r];
+                  }
+                }
+                fin_push(fin_doc, fin_sum, nfin, cur, sum);
+              }
+              cur = dg;
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                rm[r] = -INFINITY;
+                ra[r] = INT_MAX;
+              }
+            }
+            if (has_col) {
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                const int col = tid + 128 * r;
+                if (col < NC) {
+                  const float v2 = pv[w * NC + col];
+                  if (ARGMAX) {
+                    const int i2 = pi[w * NC + col];
+                    if (v2 > rm[r] || (v2 == rm[r] && i2 < ra[r])) {
+                      rm[r] = v2;
+                      ra[r] = i2;
+                    }
+                  } else {
+                    rm[r] = fmaxf(rm[r], v2);
+                  }
+                }
+              }
+            }
+          }
+          if (pass_end && cur >= 0) {
+            float sum = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const int col = tid + 128 * r;
+              const int qc = c * NC + col;
+              if (has_col && col < NC && qc < p.nq) {
+                sum += rm[r];
+                if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + cur) * p.nq + qc] = ra[r];
+              }
+            }
+            fin_push(fin_doc, fin_sum, nfin, cur, sum);
+            cur = -1;
+          }
+          // sum the finished documents' maxima over the query tokens
+          if (nfin > 0) {
+#pragma unroll
+            for (int f = 0; f < kMaxFin; ++f) {
+              if (f < nfin) {
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) fin_sum[f] += __shfl_xor_sync(0xffffffffu, fin_sum[f], o);
+              }
+            }
+            if (NC <= 32) {
+              if (tid < nfin) {
+                float total = 0.f;
+#pragma unroll
+                for (int f = 0; f < kMaxFin; ++f)
+                  if (f == tid) total = fin_sum[f];
+                int64_t b = 0;
+#pragma unroll
+                for (int f = 0; f < kMaxFin; ++f)
+                  if (f == tid) b = fin_doc[f];
+                const int64_t o = static_cast<int64_t>(q) * p.B + b;
+                if (p.n_chunks == 1) {
+                  p.out[o] = total;
+                } else {
+                  const int dl = static_cast<int>(b - first);
+                  const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
+                  if (last_chunk) p.out[o] = g2; else sm.gsum[dl] = g2;
+                }
               }
             } else {
-              rm[g] = fmaxf(rm[g], bv);
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.accempty[a]);
-          ++acc;
-        }
-        // Combine the four warps' partial maxima, then sum the query tokens.
-        float* rv = sm.red_v + rb * 4 * NC;
-        int32_t* ri = sm.red_i + rb * 4 * NC;
+              float* ps = sm.psum + pb * 4 * kMaxFin;
+              if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          rv[warp * NC + g * 32 + lane] = rm[g];
-          if (ARGMAX) ri[warp * NC + g * 32 + lane] = ra[g];
-        }
-        named_bar_sync(1, 128);
-        float part = 0.f;
-        for (int col = tid; col < NC; col += 128) {
-          float bv = rv[col];
-          int bi = ARGMAX ? ri[col] : 0;
-#pragma unroll
-          for (int w = 1; w < 4; ++w) {
-            const float v2 = rv[w * NC + col];
-            if (ARGMAX) {
-              const int i2 = ri[w * NC + col];
-              if (v2 > bv || (v2 == bv && i2 < bi)) {
-                bv = v2;
-                bi = i2;
+                for (int f = 0; f < kMaxFin; ++f)
+                  if (f < nfin) ps[warp * kMaxFin + f] = fin_sum[f];
               }
-            } else {
-              bv = fmaxf(bv, v2);
+              named_bar_sync(2, 128);
+              if (tid < nfin) {
+                const float total = (ps[0 * kMaxFin + tid] + ps[1 * kMaxFin + tid]) +
+                                    (ps[2 * kMaxFin + tid] + ps[3 * kMaxFin + tid]);
+                int64_t b = 0;
+#pragma unroll
+                for (int f = 0; f < kMaxFin; ++f)
+                  if (f == tid) b = fin_doc[f];
+                const int64_t o = static_cast<int64_t>(q) * p.B + b;
+                if (p.n_chunks == 1) {
+                  p.out[o] = total;
+                } else {
+                  const int dl = static_cast<int>(b - first);
+                  const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
+                  if (last_chunk) p.out[o] = g2; else sm.gsum[dl] = g2;
+                }
+              }
             }
           }
-          const int qc = c * NC + col;
-          if (qc < p.nq) {
-            part += bv;
-            if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + b) * p.nq + qc] = bi;
-          }
+          pb ^= 1;
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (NC <= 32) {
-          if (tid == 0) qsum += part;
-        } else {
-          if (lane == 0) sm.sred[rb * 4 + warp] = part;
-          named_bar_sync(2, 128);
-          if (tid == 0) qsum += (sm.sred[rb * 4 + 0] + sm.sred[rb * 4 + 1]) + (sm.sred[rb * 4 + 2] + sm.sred[rb * 4 + 3]);
-        }
-        rb ^= 1;
       }
-      if (tid == 0) p.out[static_cast<int64_t>(q) * p.B + b] = qsum;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_a(br.tabempty + 8 * buf);
+  }
+  // end of work: the last document of a single-pass walk is still open
+  if (!p.multipass && cur >= 0) {
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int col = tid + 128 * r;
+      if (has_col && col < NC && col < p.nq) {
+        sum += rm[r];
+        if (ARGMAX) p.argmax[cur * p.nq + col] = ra[r];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (NC <= 32) {
+      if (tid == 0) p.out[cur] = sum;
+    } else {
+      named_bar_sync(1, 128);  // earlier readers of psum are done
+      if (lane == 0) sm.psum[warp] = sum;
+      named_bar_sync(2, 128);
+      if (tid == 0) p.out[cur] = (sm.psum[0] + sm.psum[1]) + (sm.psum[2] + sm.psum[3]);
     }
   }
 }
@@ -410,22 +714,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NC = 32 * NG;
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw, p, NC);
+  const Bars br(sm, p.stages, p.n_acc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(sm.bars + s, 1);                 // full
+      mbar_init(sm.bars + p.stages + s, 1);      // empty
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.qfull[i], 1);
-      mbar_init(&sm.qempty[i], 1);
-    }
-    for (int a = 0; a < p.n_acc; ++a) {
-      mbar_init(&sm.accfull[a], 1);
-      mbar_init(&sm.accempty[a], 4);  // one arrival per epilogue warp
-    }
-    mbar_init(sm.done, 1);
+    uint64_t* rest = sm.bars + 2 * p.stages;
+    for (int i = 0; i < 4; ++i) mbar_init(rest + i, 1);                    // qfull[2], qempty[2]
+    for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + i, 1);          // accfull
+    for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + p.n_acc + i, 4);  // accempty: one per epilogue warp
+    for (int i = 0; i < 2; ++i) mbar_init(rest + 4 + 2 * p.n_acc + i, 1);  // tabfull
+    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 5);  // tabempty: MMA + 4 epilogue warps
+    mbar_init(rest + 8 + 2 * p.n_acc, 1);                                  // done
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -447,11 +750,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t b1 = (p.B * (blockIdx.x + 1)) / gridDim.x;
 
   if (warp == 4) {
-    if (lane == 0) run_producer<NC>(p, sm, &tm_d128, &tm_d32, &tm_q, b0, b1);
+    run_producer<NC>(p, sm, br, &tm_d128, &tm_d32, &tm_q, b0, b1);
   } else if (warp == 5) {
-    if (lane == 0) run_mma<NC>(p, sm, tmem_base, b0, b1);
+    if (lane == 0) run_mma<NC>(p, sm, br, tmem_base);
   } else {
-    run_epilogue<NG, ARGMAX>(p, sm, tmem_base, b0, b1);
+    run_epilogue<NG, ARGMAX>(p, sm, br, tmem_base);
   }
 
   tc_fence_before();
@@ -481,34 +784,36 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
   if (d % 64 != 0 || d < 64 || d > 1024) return MAXSIM_ERR_UNSUPPORTED;
-  if (total_rows < 1 || total_rows > static_cast<int64_t>(INT_MAX)) return MAXSIM_ERR_UNSUPPORTED;
+  // rows are int32 TMA coordinates and chunk indices are packed above 6 bits
+  if (total_rows < 1 || total_rows > (static_cast<int64_t>(1) << 30)) return MAXSIM_ERR_UNSUPPORTED;
   const int KB = d / 64;
 
   // Query chunk width NC = 32 * NG: as wide as nq needs (up to 256 columns,
-  // the largest N of one MMA), but the resident query chunk stays <= 96 KB.
-  int ng_need = (nq + 31) / 32;
+  // the largest N of one MMA), with the resident query chunk <= 96 KB.
+  const int ng_need = (nq + 31) / 32;
   int ng_cap = static_cast<int>((96 * 1024) / (static_cast<size_t>(KB) * 4096));
   if (ng_cap < 1) ng_cap = 1;
   int NG = 1;
   while (NG < ng_need && NG < 8 && NG * 2 <= ng_cap) NG *= 2;
   const int NC = 32 * NG;
   const int n_chunks = (nq + NC - 1) / NC;
+  const int multipass = (n_queries * n_chunks > 1) ? 1 : 0;
+  // multi-pass groups hold whole documents of at most 256 chunks
+  if (multipass && !csr && nd > kCapSlots * kSlotRows) return MAXSIM_ERR_UNSUPPORTED;
   const int n_acc = (512 / NC) < kMaxAcc ? (512 / NC) : kMaxAcc;
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(n_acc * NC)) tmem_cols <<= 1;
 
   const size_t budget = static_cast<size_t>(dev->max_smem_optin);
-  const size_t qslot = static_cast<size_t>(KB) * NC * 128;
   int n_qslots = 1;
-  if (n_queries * n_chunks > 1 && smem_bytes_for(NC, KB, 6, n_acc, 2) <= budget) n_qslots = 2;
+  if (multipass && smem_bytes_for(NC, KB, 6, n_acc, 2) <= budget) n_qslots = 2;
   int stages = 16;
   while (stages > 2 && smem_bytes_for(NC, KB, stages, n_acc, n_qslots) > budget) --stages;
   const size_t smem = smem_bytes_for(NC, KB, stages, n_acc, n_qslots);
   if (smem > budget) return MAXSIM_ERR_UNSUPPORTED;
-  (void)qslot;
 
-  // TMA descriptors: documents as a [total_rows, d] matrix (two box heights)
-  // and queries as [n_queries, nq, d] so rows past nq read as zero.
+  // TMA descriptors: documents as a [total_rows, d] matrix (128- and 32-row
+  // boxes) and queries as [n_queries, nq, d] so rows past nq read as zero.
   alignas(64) CUtensorMap tm_d128, tm_d32, tm_q;
   const int dt = is_bf16 ? 1 : 0;
   const uint64_t ddims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(total_rows)};
@@ -533,6 +838,7 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   p.nq = nq;
   p.KB = KB;
   p.n_chunks = n_chunks;
+  p.multipass = multipass;
   p.stages = stages;
   p.n_acc = n_acc;
   p.n_qslots = n_qslots;

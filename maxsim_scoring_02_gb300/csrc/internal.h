@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/maxsim.h"
+#include "maxsim.h"
 
 namespace msim {
 

@@ -246,3 +246,63 @@ def test_headline_size_sampled():
     perm = torch.randperm(128, device=DEV)
     out2 = m.maxsim_score(Q, D[:2048][:, perm].contiguous())
     assert torch.allclose(out2, out[:, :2048], atol=2e-6, rtol=0)
+
+
+def _check_sampled(out, am, Q, docs_of, idx, tol):
+    """Oracle on a sample of documents; docs_of(b) -> fp64 [L_b, d]."""
+    Qn = _np(Q if Q.dim() == 3 else Q[None])
+    for b in idx:
+        rows = docs_of(b)
+        ref, ref_am, gap = oracle.maxsim(Qn, rows[None] if rows.shape[0] else np.zeros((1, 1, Qn.shape[-1])),
+                                         None if rows.shape[0] else [0], want_gap=True)
+        got = out[:, b]
+        assert np.abs(got - ref[:, 0]).max() <= tol, (b, got, ref[:, 0])
+        if am is not None:
+            norms = np.linalg.norm(rows, axis=1).max() if rows.shape[0] else 1.0
+            eps = P.eps_rows(Qn, np.array([norms]), Qn.shape[-1])
+            P.check_argmax(am[:, b:b + 1], ref_am, gap, eps)
+
+
+def test_long_documents_split_across_groups():
+    """Single query: documents longer than one 256-chunk group (8192 tokens)
+    continue across groups with their running maxima intact."""
+    B, nd, d = 3, 9000, 64
+    Q = workloads.normalized_tokens((32, d), seed=91, dtype="bf16")
+    D = workloads.normalized_tokens((B, nd, d), seed=92, dtype="bf16")
+    L = torch.tensor([9000, 8193, 300], dtype=torch.int32)
+    _run_padded(Q, D, L, P.TOL_LOWP)
+
+
+def test_many_short_csr_documents():
+    """Thousands of 1..40-token documents: many groups per CTA, many documents
+    per tile, empty documents interleaved."""
+    B = 6000
+    L = workloads.uniform_lengths(B, 0, 40, seed=93)
+    off = workloads.csr_offsets(L)
+    Q = workloads.normalized_tokens((32, 128), seed=94, dtype="bf16")
+    Dp = workloads.normalized_tokens((int(off[-1]), 128), seed=95, dtype="bf16")
+    out, am = m.maxsim_score_varlen(Q.to(DEV), Dp.to(DEV), off.to(DEV), want_argmax=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    Qn, Dn, offn = _np(Q)[None], _np(Dp), off.numpy()
+    ref, ref_am, gap = oracle.maxsim_varlen(Qn, Dn, offn, want_gap=True)
+    P.check_scores(out.cpu().numpy(), ref, P.TOL_LOWP)
+    norms = np.array([np.linalg.norm(Dn[offn[b]:offn[b + 1]], axis=1).max() if offn[b + 1] > offn[b] else 1.0
+                      for b in range(B)])
+    P.check_argmax(am.cpu().numpy(), ref_am, gap, P.eps_rows(Qn, norms, 128))
+
+
+@pytest.mark.parametrize("nq", [32, 300])
+def test_multi_query_many_groups(nq):
+    """Several queries over CTA ranges of > 256 documents: several groups, each
+    scored for every (query, query chunk) pass; sampled against the oracle."""
+    B, nd = 50_000, 32
+    Q = workloads.normalized_tokens((2, nq, 128), seed=96, dtype="bf16", device=DEV)
+    D = workloads.normalized_tokens((B, nd, 128), seed=97, dtype="bf16", device=DEV)
+    L = workloads.uniform_lengths(B, 0, nd, seed=98, device=DEV)
+    out, am = m.maxsim_score(Q, D, L, want_argmax=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    idx = torch.randperm(B, generator=torch.Generator().manual_seed(7))[:300].tolist() + [0, B - 1]
+    Lc = L.cpu().numpy()
+    _check_sampled(out.cpu().numpy(), am.cpu().numpy(), Q, lambda b: _np(D[b, :Lc[b]]), idx, P.TOL_LOWP)
