@@ -28,13 +28,15 @@
 //    query tokens, K = 16; every 64-wide d-slice of a tile accumulates into
 //    the same TMEM accumulator before any maximum is taken (TileMaxSim §2(2),
 //    dimension tiling). Up to four accumulators let it run ahead.
-//  * Epilogue (warps 0-3): tcgen05.ld of the warp's 32 lanes, rows past the
-//    chunk's valid rows masked to -inf, a transpose butterfly of shuffles
+//  * Slot partials (warps 0-3): tcgen05.ld of the warp's 32 lanes, rows past
+//    the chunk's valid rows masked to -inf, a transpose butterfly of shuffles
 //    leaves lane l with the maximum (and lowest argmax) of query column l
-//    over the slot; slot partials are merged in document order through shared
-//    memory and each finished document's maxima are summed (FLASH-MAXSIM
-//    Figure 1: only the scalar score is written). The similarity tile exists
-//    only in TMEM and registers.
+//    over the slot, handed over in a ring of shared-memory buffers.
+//  * Merge (warp 6): folds slot partials in document order and, when a
+//    document ends, sums its per-token maxima and writes the score
+//    (FLASH-MAXSIM Figure 1: only the scalar score is written). Partial
+//    warps never wait for the merge except through the buffer ring. The
+//    similarity tile exists only in TMEM and registers.
 //  * Every mbarrier wait is bounded (ptx.cuh); after an abort the producer
 //    drains its in-flight TMA loads and the MMA thread waits for its last MMA
 //    before TMEM is released.
@@ -50,7 +52,7 @@
 namespace msim {
 namespace {
 
-constexpr int kThreads = 192;        // warps 0-3 epilogue, 4 producer, 5 MMA
+constexpr int kThreads = 224;        // warps 0-3 slot partials, 4 producer, 5 MMA, 6 merge
 constexpr int kStageBytes = 16384;   // 128 rows x 64 elements x 2 bytes
 constexpr int kSlotRows = 32;
 constexpr int kCapSlots = 256;       // chunk slots per group table
@@ -73,6 +75,7 @@ struct FwdTcParams {
   int stages;
   int n_acc;
   int n_qslots;
+  int n_part;      // slot-partial buffers between the partial warps and the merge warp
   uint32_t idesc;
   uint32_t tmem_cols;
   float* out;
@@ -95,26 +98,27 @@ struct Smem {
   uint8_t* q;            // n_qslots x KB boxes of NC rows x 128 B
   uint8_t* stages;       // stages x 16 KB
   GroupTab* tab;         // [2]
-  uint64_t* bars;        // full[S] empty[S] qfull[2] qempty[2] accfull[A] accempty[A] tabfull[2] tabempty[2] done
+  uint64_t* bars;        // full[S] empty[S] qfull[2] qempty[2] accfull[A] accempty[A] tabfull[2] tabempty[2]
+                         // partfull[PB] partempty[PB] done
   uint32_t* tmem_slot;
   volatile int* abort_flag;
-  float* part_v;         // [2][4][NC]
-  int32_t* part_i;       // [2][4][NC]
-  float* psum;           // [2][4][kMaxFin]
+  float* part_v;         // [PB][4][NC]
+  int32_t* part_i;       // [PB][4][NC]
   float* gsum;           // [kCapDocs]
 };
 
-__host__ __device__ inline size_t bars_count(int stages, int n_acc) { return 2 * stages + 4 + 2 * n_acc + 4 + 1; }
+__host__ __device__ inline size_t bars_count(int stages, int n_acc, int n_part) {
+  return 2 * stages + 4 + 2 * n_acc + 4 + 2 * n_part + 1;
+}
 
-__host__ __device__ inline size_t smem_bytes_for(int NC, int KB, int stages, int n_acc, int n_qslots) {
+__host__ __device__ inline size_t smem_bytes_for(int NC, int KB, int stages, int n_acc, int n_qslots, int n_part) {
   size_t bytes = 1024;  // alignment slack for the dynamic region
   bytes += static_cast<size_t>(n_qslots) * KB * NC * 128;
   bytes += static_cast<size_t>(stages) * kStageBytes;
   bytes += 2 * sizeof(GroupTab);
-  bytes += bars_count(stages, n_acc) * 8;
+  bytes += bars_count(stages, n_acc, n_part) * 8;
   bytes += 16;
-  bytes += static_cast<size_t>(2 * 4 * NC) * 8;
-  bytes += 2 * 4 * kMaxFin * 4;
+  bytes += static_cast<size_t>(n_part * 4 * NC) * 8;
   bytes += kCapDocs * 4;
   return bytes;
 }
@@ -126,19 +130,18 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const FwdTcParams& p, int NC
   s.stages = s.q + static_cast<size_t>(p.n_qslots) * p.KB * NC * 128;
   s.tab = reinterpret_cast<GroupTab*>(s.stages + static_cast<size_t>(p.stages) * kStageBytes);
   s.bars = reinterpret_cast<uint64_t*>(s.tab + 2);
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + bars_count(p.stages, p.n_acc));
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + bars_count(p.stages, p.n_acc, p.n_part));
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
   s.part_v = reinterpret_cast<float*>(s.tmem_slot + 4);
-  s.part_i = reinterpret_cast<int32_t*>(s.part_v + 2 * 4 * NC);
-  s.psum = reinterpret_cast<float*>(s.part_i + 2 * 4 * NC);
-  s.gsum = s.psum + 2 * 4 * kMaxFin;
+  s.part_i = reinterpret_cast<int32_t*>(s.part_v + p.n_part * 4 * NC);
+  s.gsum = reinterpret_cast<float*>(s.part_i + p.n_part * 4 * NC);
   return s;
 }
 
 // Barrier addresses (32-bit shared) in the order laid out by carve().
 struct Bars {
-  uint32_t full, empty, qfull, qempty, accfull, accempty, tabfull, tabempty, done;
-  __device__ __forceinline__ Bars(const Smem& sm, int S, int A) {
+  uint32_t full, empty, qfull, qempty, accfull, accempty, tabfull, tabempty, partfull, partempty, done;
+  __device__ __forceinline__ Bars(const Smem& sm, int S, int A, int PB) {
     const uint32_t b0 = smem_u32(sm.bars);
     full = b0;
     empty = full + 8 * S;
@@ -148,7 +151,9 @@ struct Bars {
     accempty = accfull + 8 * A;
     tabfull = accempty + 8 * A;
     tabempty = tabfull + 16;
-    done = tabempty + 16;
+    partfull = tabempty + 16;
+    partempty = partfull + 8 * PB;
+    done = partempty + 8 * PB;
   }
 };
 
@@ -475,27 +480,110 @@ __device__ __forceinline__ void fin_push(int64_t (&fd)[kMaxFin], float (&fs)[kMa
   ++n;
 }
 
-// ------------------------------------------------------------ epilogue warps
+// --------------------------------------------------------- partial warps 0-3
+// Warp w reduces slot w of every tile: TMEM lanes 32w..32w+31 hold 32 rows of
+// one document; the butterfly leaves the slot's per-column maxima in
+// part[pbuf][w][:], handed to the merge warp through partfull/partempty.
 template <int NG, bool ARGMAX>
-__device__ void run_epilogue(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
+__device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
   constexpr int NC = 32 * NG;
-  constexpr int R = NC > 128 ? 2 : 1;   // merge columns per thread
-  const int tid = threadIdx.x;          // 0..127 == TMEM lane
+  const int tid = threadIdx.x;  // 0..127 == TMEM lane
   const int warp = tid >> 5, lane = tid & 31;
-  const int A = p.n_acc;
+  const int A = p.n_acc, PB = p.n_part;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const bool has_col = tid < NC;
   int a = 0, pb = 0;
-  uint32_t aph = 0;
-  // running state of the current document for this thread's merge columns
-  int64_t cur = -1;
-  float rm[R];
-  int ra[R];
+  uint32_t aph = 0, pph = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    const int buf = gi & 1;
+    if (!mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) return;
+    const GroupTab* T = sm.tab + buf;
+    if (T->n_docs < 0) break;
+    const int n_slots = T->n_slots;
+    const int n_tiles = (n_slots + 3) >> 2;
+    const int passes = p.n_queries * p.n_chunks;
+    for (int pass = 0; pass < passes; ++pass) {
+      for (int t = 0; t < n_tiles; ++t) {
+        if (!mbar_wait_a(br.partempty + 8 * pb, pph ^ 1u, sm.abort_flag, p.status)) return;
+        if (!mbar_wait_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
+        tc_fence_after();
+        const int i0 = 4 * t;
+        if (warp < n_slots - i0) {
+          const int info = T->slot_info[i0 + warp];
+          const int vrows = info & 63;
+          const int row = (info >> 6) * kSlotRows + lane;   // doc-local token index of this lane's row
+          float* pv = sm.part_v + (pb * 4 + warp) * NC;
+          int32_t* pi = sm.part_i + (pb * 4 + warp) * NC;
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    rm[r] = -INFINITY;
-    ra[r] = INT_MAX;
+          for (int g = 0; g < NG; ++g) {
+            float v[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(a * NC + g * 32), v);
+            if (g == NG - 1) {  // accumulator fully in registers: hand it back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
+            }
+            if (lane >= vrows) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] = -INFINITY;
+            }
+            float bv;
+            int bi;
+            warp_column_max<ARGMAX>(v, row, lane, bv, bi);
+            pv[g * 32 + lane] = bv;
+            if (ARGMAX) pi[g * 32 + lane] = bi;
+          }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
+        }
+        mbar_arrive_a(br.partfull + 8 * pb);  // every partial thread arrives (count 128)
+        if (++a == A) {
+          a = 0;
+          aph ^= 1u;
+        }
+        if (++pb == PB) {
+          pb = 0;
+          pph ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_a(br.tabempty + 8 * buf);
   }
+}
+
+// --------------------------------------------------------------- merge warp
+// Merges slot partials in document order (lane l owns query columns
+// l, l+32, ...), finishes documents (sum over query tokens, argmax), and
+// writes empty documents' outputs.
+template <int NG, bool ARGMAX>
+__device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) {
+  constexpr int NC = 32 * NG;
+  const int lane = threadIdx.x & 31;
+  const int PB = p.n_part;
+  int pb = 0;
+  uint32_t pph = 0;
+  int64_t cur = -1;
+  float rm[NG];
+  int ra[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    rm[g] = -INFINITY;
+    ra[g] = INT_MAX;
+  }
+  auto doc_sum = [&](int c, int64_t doc, int q) -> float {
+    float sum = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int qc = c * NC + g * 32 + lane;
+      if (qc < p.nq) {
+        sum += rm[g];
+        if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + doc) * p.nq + qc] = ra[g];
+      }
+    }
+    return sum;
+  };
   for (uint32_t gi = 0;; ++gi) {
     const int buf = gi & 1;
     if (!mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) return;
@@ -509,7 +597,7 @@ __device__ void run_epilogue(const FwdTcParams& p, const Smem& sm, const Bars& b
       for (int c = 0; c < p.n_chunks; ++c) {
         const bool last_chunk = c == p.n_chunks - 1;
         // empty documents of the group: score 0, argmax -1 (no slots, no MMA)
-        for (int dl = tid; dl < n_docs; dl += 128) {
+        for (int dl = lane; dl < n_docs; dl += 32) {
           if (T->doc_len[dl] == 0) {
             const int64_t b = first + dl;
             if (ARGMAX)
@@ -522,161 +610,75 @@ __device__ void run_epilogue(const FwdTcParams& p, const Smem& sm, const Bars& b
         }
         if (p.multipass) cur = -1;
         for (int t = 0; t < n_tiles; ++t) {
-          if (!mbar_wait_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
-          tc_fence_after();
+          if (!mbar_wait_a(br.partfull + 8 * pb, pph, sm.abort_flag, p.status)) return;
           const int i0 = 4 * t;
           const int nslot = min(4, n_slots - i0);
-          float* pv = sm.part_v + pb * 4 * NC;
-          int32_t* pi = sm.part_i + pb * 4 * NC;
-          if (warp < nslot) {
-            const int info = T->slot_info[i0 + warp];
-            const int vrows = info & 63;
-            const int row = (info >> 6) * kSlotRows + lane;   // doc-local token index of this lane's row
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-              float v[32];
-              tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(a * NC + g * 32), v);
-              if (g == NG - 1) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
-              }
-              if (lane >= vrows) {
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = -INFINITY;
-              }
-              float bv;
-              int bi;
-              warp_column_max<ARGMAX>(v, row, lane, bv, bi);
-              pv[warp * NC + g * 32 + lane] = bv;
-              if (ARGMAX) pi[warp * NC + g * 32 + lane] = bi;
-            }
-          } else {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
-          }
-          if (++a == A) {
-            a = 0;
-            aph ^= 1u;
-          }
-          named_bar_sync(1, 128);
-          // merge the slot partials in document order; collect finished documents
           int nfin = 0;
           int64_t fin_doc[kMaxFin];
           float fin_sum[kMaxFin];
-          const bool pass_end = p.multipass && (t == n_tiles - 1);
+          const float* pv = sm.part_v + pb * 4 * NC;
+          const int32_t* pi = sm.part_i + pb * 4 * NC;
           for (int w = 0; w < nslot; ++w) {
             const int64_t dg = first + T->slot_doc[i0 + w];
             if (dg != cur) {
-              if (cur >= 0) {
-                float sum = 0.f;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                  const int col = tid + 128 * r;
-                  const int qc = c * NC + col;
-                  if (has_col && col < NC && qc < p.nq) {
-                    sum += rm[r];
-                    if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + cur) * p.nq + qc] = ra[r];
-                  }
-                }
-                fin_push(fin_doc, fin_sum, nfin, cur, sum);
-              }
+              if (cur >= 0) fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, cur, q));
               cur = dg;
 #pragma unroll
-              for (int r = 0; r < R; ++r) {
-                rm[r] = -INFINITY;
-                ra[r] = INT_MAX;
+              for (int g = 0; g < NG; ++g) {
+                rm[g] = -INFINITY;
+                ra[g] = INT_MAX;
               }
             }
-            if (has_col) {
 #pragma unroll
-              for (int r = 0; r < R; ++r) {
-                const int col = tid + 128 * r;
-                if (col < NC) {
-                  const float v2 = pv[w * NC + col];
-                  if (ARGMAX) {
-                    const int i2 = pi[w * NC + col];
-                    if (v2 > rm[r] || (v2 == rm[r] && i2 < ra[r])) {
-                      rm[r] = v2;
-                      ra[r] = i2;
-                    }
-                  } else {
-                    rm[r] = fmaxf(rm[r], v2);
-                  }
+            for (int g = 0; g < NG; ++g) {
+              const float v2 = pv[w * NC + g * 32 + lane];
+              if (ARGMAX) {
+                const int i2 = pi[w * NC + g * 32 + lane];
+                if (v2 > rm[g] || (v2 == rm[g] && i2 < ra[g])) {
+                  rm[g] = v2;
+                  ra[g] = i2;
                 }
+              } else {
+                rm[g] = fmaxf(rm[g], v2);
               }
             }
           }
-          if (pass_end && cur >= 0) {
-            float sum = 0.f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              const int col = tid + 128 * r;
-              const int qc = c * NC + col;
-              if (has_col && col < NC && qc < p.nq) {
-                sum += rm[r];
-                if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + cur) * p.nq + qc] = ra[r];
-              }
-            }
-            fin_push(fin_doc, fin_sum, nfin, cur, sum);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(br.partempty + 8 * pb);
+          if (++pb == PB) {
+            pb = 0;
+            pph ^= 1u;
+          }
+          if (p.multipass && t == n_tiles - 1 && cur >= 0) {
+            fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, cur, q));
             cur = -1;
           }
-          // sum the finished documents' maxima over the query tokens
           if (nfin > 0) {
 #pragma unroll
-            for (int f = 0; f < kMaxFin; ++f) {
+            for (int f = 0; f < kMaxFin; ++f)
               if (f < nfin) {
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) fin_sum[f] += __shfl_xor_sync(0xffffffffu, fin_sum[f], o);
               }
-            }
-            if (NC <= 32) {
-              if (tid < nfin) {
-                float total = 0.f;
+            if (lane < nfin) {
+              float total = 0.f;
+              int64_t b = 0;
 #pragma unroll
-                for (int f = 0; f < kMaxFin; ++f)
-                  if (f == tid) total = fin_sum[f];
-                int64_t b = 0;
-#pragma unroll
-                for (int f = 0; f < kMaxFin; ++f)
-                  if (f == tid) b = fin_doc[f];
-                const int64_t o = static_cast<int64_t>(q) * p.B + b;
-                if (p.n_chunks == 1) {
-                  p.out[o] = total;
-                } else {
-                  const int dl = static_cast<int>(b - first);
-                  const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
-                  if (last_chunk) p.out[o] = g2; else sm.gsum[dl] = g2;
+              for (int f = 0; f < kMaxFin; ++f)
+                if (f == lane) {
+                  total = fin_sum[f];
+                  b = fin_doc[f];
                 }
-              }
-            } else {
-              float* ps = sm.psum + pb * 4 * kMaxFin;
-              if (lane == 0) {
-#pragma unroll
-                for (int f = 0; f < kMaxFin; ++f)
-                  if (f < nfin) ps[warp * kMaxFin + f] = fin_sum[f];
-              }
-              named_bar_sync(2, 128);
-              if (tid < nfin) {
-                const float total = (ps[0 * kMaxFin + tid] + ps[1 * kMaxFin + tid]) +
-                                    (ps[2 * kMaxFin + tid] + ps[3 * kMaxFin + tid]);
-                int64_t b = 0;
-#pragma unroll
-                for (int f = 0; f < kMaxFin; ++f)
-                  if (f == tid) b = fin_doc[f];
-                const int64_t o = static_cast<int64_t>(q) * p.B + b;
-                if (p.n_chunks == 1) {
-                  p.out[o] = total;
-                } else {
-                  const int dl = static_cast<int>(b - first);
-                  const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
-                  if (last_chunk) p.out[o] = g2; else sm.gsum[dl] = g2;
-                }
+              const int64_t o = static_cast<int64_t>(q) * p.B + b;
+              if (p.n_chunks == 1) {
+                p.out[o] = total;
+              } else {
+                const int dl = static_cast<int>(b - first);
+                const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
+                if (last_chunk) p.out[o] = g2; else sm.gsum[dl] = g2;
               }
             }
           }
-          pb ^= 1;
         }
       }
     }
@@ -685,25 +687,10 @@ __device__ void run_epilogue(const FwdTcParams& p, const Smem& sm, const Bars& b
   }
   // end of work: the last document of a single-pass walk is still open
   if (!p.multipass && cur >= 0) {
-    float sum = 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int col = tid + 128 * r;
-      if (has_col && col < NC && col < p.nq) {
-        sum += rm[r];
-        if (ARGMAX) p.argmax[cur * p.nq + col] = ra[r];
-      }
-    }
+    float sum = doc_sum(0, cur, 0);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (NC <= 32) {
-      if (tid == 0) p.out[cur] = sum;
-    } else {
-      named_bar_sync(1, 128);  // earlier readers of psum are done
-      if (lane == 0) sm.psum[warp] = sum;
-      named_bar_sync(2, 128);
-      if (tid == 0) p.out[cur] = (sm.psum[0] + sm.psum[1]) + (sm.psum[2] + sm.psum[3]);
-    }
+    if (lane == 0) p.out[cur] = sum;
   }
 }
 
@@ -714,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NC = 32 * NG;
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw, p, NC);
-  const Bars br(sm, p.stages, p.n_acc);
+  const Bars br(sm, p.stages, p.n_acc, p.n_part);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -727,8 +714,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + i, 1);          // accfull
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + p.n_acc + i, 4);  // accempty: one per epilogue warp
     for (int i = 0; i < 2; ++i) mbar_init(rest + 4 + 2 * p.n_acc + i, 1);  // tabfull
-    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 5);  // tabempty: MMA + 4 epilogue warps
-    mbar_init(rest + 8 + 2 * p.n_acc, 1);                                  // done
+    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 6);  // tabempty: MMA + 4 partial + merge
+    uint64_t* pr = rest + 8 + 2 * p.n_acc;
+    for (int i = 0; i < p.n_part; ++i) mbar_init(pr + i, 128);             // partfull: every partial thread
+    for (int i = 0; i < p.n_part; ++i) mbar_init(pr + p.n_part + i, 1);    // partempty: merge warp
+    mbar_init(pr + 2 * p.n_part, 1);                                       // done
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -753,8 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     run_producer<NC>(p, sm, br, &tm_d128, &tm_d32, &tm_q, b0, b1);
   } else if (warp == 5) {
     if (lane == 0) run_mma<NC>(p, sm, br, tmem_base);
+  } else if (warp == 6) {
+    run_merge<NG, ARGMAX>(p, sm, br);
   } else {
-    run_epilogue<NG, ARGMAX>(p, sm, br, tmem_base);
+    run_partials<NG, ARGMAX>(p, sm, br, tmem_base);
   }
 
   tc_fence_before();
@@ -805,11 +797,12 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   while (tmem_cols < static_cast<uint32_t>(n_acc * NC)) tmem_cols <<= 1;
 
   const size_t budget = static_cast<size_t>(dev->max_smem_optin);
+  const int n_part = NC >= 128 ? 2 : 4;
   int n_qslots = 1;
-  if (multipass && smem_bytes_for(NC, KB, 6, n_acc, 2) <= budget) n_qslots = 2;
+  if (multipass && smem_bytes_for(NC, KB, 6, n_acc, 2, n_part) <= budget) n_qslots = 2;
   int stages = 16;
-  while (stages > 2 && smem_bytes_for(NC, KB, stages, n_acc, n_qslots) > budget) --stages;
-  const size_t smem = smem_bytes_for(NC, KB, stages, n_acc, n_qslots);
+  while (stages > 2 && smem_bytes_for(NC, KB, stages, n_acc, n_qslots, n_part) > budget) --stages;
+  const size_t smem = smem_bytes_for(NC, KB, stages, n_acc, n_qslots, n_part);
   if (smem > budget) return MAXSIM_ERR_UNSUPPORTED;
 
   // TMA descriptors: documents as a [total_rows, d] matrix (128- and 32-row
@@ -842,6 +835,7 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   p.stages = stages;
   p.n_acc = n_acc;
   p.n_qslots = n_qslots;
+  p.n_part = n_part;
   p.idesc = idesc_f16(is_bf16, 128, NC);
   p.tmem_cols = tmem_cols;
   p.out = out;
