@@ -139,9 +139,14 @@ maxsim_status maxsim_score_varlen(const void *Q, int n_queries, int nq, int d,
  *   codebooks  [M, K, d/M] fp32 (d % M == 0, K <= 256)
  *   codes      [total_tokens, M] uint8, CSR documents as in maxsim_score_varlen
  *   out        [B] fp32; argmax_out [B, nq] int32 or NULL
- *   workspace  >= maxsim_score_pq_workspace_size(nq, M, K) bytes, 256-byte aligned
+ *   workspace  >= maxsim_score_pq_workspace_size(nq, M, K) bytes, 16-byte
+ *              aligned; holds the table (groups of 8 query tokens, fp32);
+ *              contents on entry are ignored, the call overwrites it.
  *
- * Limits: 1 <= nq <= 1024, 1 <= M <= 64, 1 <= K <= 256, d % M == 0, d <= 1024.
+ * Limits: 1 <= nq <= 1024; M % 4 == 0, 4 <= M <= 64; 1 <= K <= 256;
+ * d % M == 0, d <= 1024; M * K * 32 bytes (one 8-token table group) must fit
+ * in shared memory (M * K <= 7168). A code >= K is clamped to K-1 and sets
+ * MAXSIM_DEVERR_BAD_INPUT. Missing or short workspace: MAXSIM_ERR_WORKSPACE.
  */
 size_t maxsim_score_pq_workspace_size(int nq, int M, int K);
 maxsim_status maxsim_score_pq(const float *Q, int nq, int d,
@@ -165,7 +170,11 @@ maxsim_status maxsim_score_pq(const float *Q, int nq, int d,
  *   (dot at the argmax), argmax_out [B, nq] int32 -- each of the last three
  *   may be NULL.
  *
- * Limits: 1 <= nq <= 256, d % 64 == 0, 64 <= d <= 1024 (|dot| < 2^24).
+ * Runs on the warp-level tensor-core IMMA path (mma.sync m16n8k32 s8):
+ * the tcgen05 8-bit integer MMA is not available for sm_103a.
+ *
+ * Limits: 1 <= nq <= 256; d in {64, 128, 192, 256, 384, 512, 768, 1024}
+ * (so |dot| < 2^24 and (float)dot is exact); Q and D 16-byte aligned.
  */
 maxsim_status maxsim_score_i8(const int8_t *Q, const float *q_scale, int nq, int d,
                               const int8_t *D, const float *d_scale,

@@ -178,27 +178,47 @@ maxsim_status maxsim_score_varlen(const void* Q, int n_queries, int nq, int d, c
                        dtype == MAXSIM_BF16 ? 1 : 0, out, argmax_out, s);
 }
 
-size_t maxsim_score_pq_workspace_size(int nq, int M, int K) {
-  if (nq < 1 || M < 1 || K < 1) return 0;
-  return static_cast<size_t>(nq) * M * K * sizeof(float);
-}
+size_t maxsim_score_pq_workspace_size(int nq, int M, int K) { return pq_workspace_bytes(nq, M, K); }
 
 maxsim_status maxsim_score_pq(const float* Q, int nq, int d, const float* codebooks, int M, int K,
                               const uint8_t* codes, const int64_t* offsets, int64_t B, int64_t total_tokens,
                               float* out, int32_t* argmax_out, void* workspace, size_t workspace_bytes,
                               void* stream) {
-  (void)Q; (void)nq; (void)d; (void)codebooks; (void)M; (void)K; (void)codes; (void)offsets; (void)B;
-  (void)total_tokens; (void)out; (void)argmax_out; (void)workspace; (void)workspace_bytes; (void)stream;
-  return MAXSIM_ERR_UNSUPPORTED;
+  if (nq < 1 || nq > 1024 || d < 1 || d > 1024 || B < 0 || total_tokens < 0) return MAXSIM_ERR_INVALID_ARG;
+  if (M < 4 || M > 64 || M % 4 != 0 || K < 1 || K > 256 || d % M != 0) return MAXSIM_ERR_UNSUPPORTED;
+  if (B == 0) return MAXSIM_OK;
+  if (!Q || !codebooks || !offsets || !out || (total_tokens > 0 && !codes)) return MAXSIM_ERR_INVALID_ARG;
+  if (!aligned4(Q) || !aligned4(codebooks) || !aligned4(offsets) || !aligned4(out) ||
+      (codes && !aligned4(codes)) || (argmax_out && !aligned4(argmax_out)))
+    return MAXSIM_ERR_INVALID_ARG;
+  const size_t need = pq_workspace_bytes(nq, M, K);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MAXSIM_ERR_WORKSPACE;
+  if (!codes) codes = reinterpret_cast<const uint8_t*>(Q);  // no tokens at all: never read
+  return launch_pq(Q, nq, d, codebooks, M, K, codes, offsets, B, total_tokens, out, argmax_out,
+                   static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 maxsim_status maxsim_score_i8(const int8_t* Q, const float* q_scale, int nq, int d, const int8_t* D,
                               const float* d_scale, const int64_t* offsets, int64_t B, int64_t total_tokens,
                               float* out, float* maxv_out, int32_t* maxdot_out, int32_t* argmax_out,
                               void* stream) {
-  (void)Q; (void)q_scale; (void)nq; (void)d; (void)D; (void)d_scale; (void)offsets; (void)B; (void)total_tokens;
-  (void)out; (void)maxv_out; (void)maxdot_out; (void)argmax_out; (void)stream;
-  return MAXSIM_ERR_UNSUPPORTED;
+  if (nq < 1 || nq > 256 || d < 1 || B < 0 || total_tokens < 0) return MAXSIM_ERR_INVALID_ARG;
+  switch (d) {
+    case 64: case 128: case 192: case 256: case 384: case 512: case 768: case 1024: break;
+    default: return MAXSIM_ERR_UNSUPPORTED;
+  }
+  if (B == 0) return MAXSIM_OK;
+  if (!Q || !q_scale || !offsets || !out || (total_tokens > 0 && (!D || !d_scale))) return MAXSIM_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned4(q_scale) || !aligned4(offsets) || !aligned4(out) || (D && !aligned16(D)) ||
+      (d_scale && !aligned4(d_scale)) || (maxv_out && !aligned4(maxv_out)) ||
+      (maxdot_out && !aligned4(maxdot_out)) || (argmax_out && !aligned4(argmax_out)))
+    return MAXSIM_ERR_INVALID_ARG;
+  if (!D) {  // no tokens at all: never read
+    D = Q;
+    d_scale = q_scale;
+  }
+  return launch_i8(Q, q_scale, nq, d, D, d_scale, offsets, B, total_tokens, out, maxv_out, maxdot_out, argmax_out,
+                   static_cast<cudaStream_t>(stream));
 }
 
 size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd) {

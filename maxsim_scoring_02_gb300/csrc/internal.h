@@ -32,6 +32,18 @@ maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const
                              int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
                              float* out, int32_t* argmax, cudaStream_t stream);
 
+// Product-quantisation scoring: table build into `table` (pq_workspace_bytes
+// of device memory, 16-byte aligned), then table-lookup scoring.
+size_t pq_workspace_bytes(int nq, int M, int K);
+maxsim_status launch_pq(const float* Q, int nq, int d, const float* C, int M, int K, const uint8_t* codes,
+                        const int64_t* offsets, int64_t B, int64_t total_tokens, float* out, int32_t* argmax,
+                        float* table, cudaStream_t stream);
+
+// INT8 x INT8 scoring (warp-level IMMA, exact int32 dots).
+maxsim_status launch_i8(const int8_t* Q, const float* q_scale, int nq, int d, const int8_t* D, const float* d_scale,
+                        const int64_t* offsets, int64_t B, int64_t total_tokens, float* out, float* maxv,
+                        int32_t* maxdot, int32_t* argmax, cudaStream_t stream);
+
 // Encodes a TMA tensor map through the driver entry point (no libcuda link).
 // Returns false if the driver call is unavailable or rejects the arguments.
 bool encode_tmap(void* tmap, int dtype_code, int rank, void* gaddr, const uint64_t* dims,

@@ -1,0 +1,110 @@
+"""GPU parity: INT8 x INT8 scoring against the oracle.
+
+Both sides form sim = (float)dot * s_d[j] as one fp32 round-to-nearest
+multiply of an exact integer dot, and compare in fp32 with the lowest index
+winning ties; so the per-token maxima, their integer dots and their indices
+must match BIT-EXACTLY. The score (a sum of nq fp32 products) is checked to
+1e-5 * sum_i |s_q[i] * m_i|.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+m = pytest.importorskip("maxsim_scoring_02_gb300")
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.load_library()
+
+
+def _inputs(B, nq, d, seed, lo=8, hi=256, empty=()):
+    L = workloads.lognormal_lengths(B, math.log(70), 0.5, lo, hi, seed=seed)
+    for e in empty:
+        L[e] = 0
+    off = workloads.csr_offsets(L)
+    Qf = workloads.normalized_tokens((nq, d), seed=seed + 1, dtype="fp32")
+    Df = workloads.normalized_tokens((int(off[-1]), d), seed=seed + 2, dtype="fp32")
+    Qi, sq = workloads.quantize_int8(Qf)
+    Di, sd = workloads.quantize_int8(Df)
+    return Qi, sq, Di, sd, off
+
+
+def _check(Qi, sq, Di, sd, off):
+    out, mv, md, am = m.maxsim_score_i8(Qi.to(DEV), sq.to(DEV), Di.to(DEV), sd.to(DEV), off.to(DEV),
+                                        want_details=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    ref, rmv, rmd, ram = oracle.maxsim_i8(Qi.numpy(), sq.numpy(), Di.numpy(), sd.numpy(), off.numpy())
+    np.testing.assert_array_equal(md.cpu().numpy(), rmd)
+    np.testing.assert_array_equal(mv.cpu().numpy(), rmv)
+    np.testing.assert_array_equal(am.cpu().numpy(), ram)
+    bound = 1e-5 * np.maximum(np.abs(sq.numpy()[None, :].astype(np.float64) * rmv).sum(axis=1), 1e-30)
+    assert (np.abs(out.cpu().numpy() - ref) <= bound).all()
+    return out
+
+
+def test_golden_case_embedded_in_d64(golden_dir):
+    """The hand-derived INT8 case with d padded by zeros to 64: same dots,
+    same fp32 products, so every output equals the golden value exactly."""
+    g = json.load(open(os.path.join(golden_dir, "i8_tiny.json")))
+    Q = torch.zeros(2, 64, dtype=torch.int8)
+    Q[:, :2] = torch.tensor(g["Q"], dtype=torch.int8)
+    D = torch.zeros(3, 64, dtype=torch.int8)
+    D[:, :2] = torch.tensor(g["D"], dtype=torch.int8)
+    out, mv, md, am = m.maxsim_score_i8(Q.to(DEV), torch.tensor(g["s_q"], device=DEV), D.to(DEV),
+                                        torch.tensor(g["s_d"], device=DEV),
+                                        torch.tensor(g["offsets"], device=DEV), want_details=True)
+    assert out.cpu().tolist() == g["score"]
+    assert mv.cpu().tolist() == g["maxv"] and md.cpu().tolist() == g["maxdot"] and am.cpu().tolist() == g["argmax"]
+
+
+def test_config_shaped_i8():
+    """Per-token symmetric INT8 of L2-normalised Gaussian tokens, d=128,
+    Q[32,128], lognormal(ln 70, 0.5) lengths clipped to [8, 256]."""
+    _check(*_inputs(3000, 32, 128, seed=201, empty=(3, 2999)))
+
+
+@pytest.mark.parametrize("nq,d", [(1, 64), (20, 128), (32, 192), (45, 256), (64, 512), (100, 768), (7, 1024)])
+def test_i8_shapes(nq, d):
+    _check(*_inputs(300, nq, d, seed=nq + d, lo=1, hi=100, empty=(0,)))
+
+
+def test_extreme_values_exact():
+    """All +-127 inputs: dots reach 127^2 * d; every partial sum must stay exact."""
+    d = 1024
+    rng = np.random.default_rng(5)
+    Q = torch.tensor(rng.choice([-127, 127], size=(8, d)), dtype=torch.int8)
+    D = torch.tensor(rng.choice([-127, 127], size=(40, d)), dtype=torch.int8)
+    D[7] = Q[3]                                   # dot = 127^2 * 1024 = 16516096 < 2^24
+    sq = torch.full((8,), 1e-3)
+    sd = torch.linspace(0.5, 2.0, 40)
+    _check(Q, sq, D, sd, torch.tensor([0, 13, 40]))
+
+
+def test_i8_many_docs_sampled():
+    """B=500000 documents: 500 sampled documents checked bit-exactly."""
+    Qi, sq, Di, sd, off = _inputs(500_000, 32, 128, seed=211)
+    out, mv, md, am = m.maxsim_score_i8(Qi.to(DEV), sq.to(DEV), Di.to(DEV), sd.to(DEV), off.to(DEV),
+                                        want_details=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    idx = np.sort(np.random.default_rng(9).choice(500_000, 500, replace=False))
+    offn = off.numpy()
+    for b in idx:
+        o2 = np.array([0, offn[b + 1] - offn[b]])
+        ref, rmv, rmd, ram = oracle.maxsim_i8(Qi.numpy(), sq.numpy(), Di.numpy()[offn[b]:offn[b + 1]],
+                                              sd.numpy()[offn[b]:offn[b + 1]], o2)
+        assert (md[b].cpu().numpy() == rmd[0]).all() and (am[b].cpu().numpy() == ram[0]).all()
+        assert (mv[b].cpu().numpy() == rmv[0]).all()
