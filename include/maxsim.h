@@ -157,6 +157,37 @@ maxsim_status maxsim_score_pq(const float *Q, int nq, int d,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * maxsim_score_pq_noalloc -- maxsim_score_pq for callers that cannot
+ * allocate device memory. The source pages have no counterpart: this is a
+ * library convenience, not part of the method.
+ *
+ * Some callers have no way to hand over a workspace: code that runs where a
+ * device allocation is forbidden or unavailable (a host callback, a hook
+ * inside another library, a plugin without an allocator). This variant keeps
+ * the PQ table in a fixed 1 MiB device array compiled into the library
+ * (present on every GPU that loads it, until the process exits) and
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *
+ *   Arguments, layouts, results and other limits: as maxsim_score_pq,
+ *   without the workspace.
+ *   Limit: the table, ceil(nq/8)*8 * M * K * 4 bytes, must fit in 1 MiB
+ *   (e.g. nq <= 64 at M = 16, K = 256); larger requests return
+ *   MAXSIM_ERR_WORKSPACE before anything is launched.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address with that device current; make that first call before any
+ *   stream capture. A failed lookup returns MAXSIM_ERR_CUDA.
+ *   Sharing: every call uses the same array, and it keeps the previous
+ *   call's table. Each call rewrites every entry it reads, so no clearing is
+ *   needed; but calls whose kernels overlap on the GPU (for example on two
+ *   streams) race on the array and give wrong results -- serialise them.
+ */
+maxsim_status maxsim_score_pq_noalloc(const float *Q, int nq, int d,
+                                      const float *codebooks, int M, int K,
+                                      const uint8_t *codes, const int64_t *offsets,
+                                      int64_t B, int64_t total_tokens,
+                                      float *out, int32_t *argmax_out, void *stream);
+
+/*
  * maxsim_score_i8 -- INT8 x INT8 scoring (FLASH-MAXSIM, Abstract) with
  * per-token symmetric scales:
  *   dot(i,j) = sum_k Q[i,k] * D[j,k]        exact int32

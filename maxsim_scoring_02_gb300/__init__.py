@@ -38,7 +38,8 @@ DEVERR_BAD_INPUT = 0x2
 # Every symbol the header declares (checked by the tests).
 EXPORTS = (
     "maxsim_version", "maxsim_status_string", "maxsim_device_status", "maxsim_score",
-    "maxsim_score_varlen", "maxsim_score_pq_workspace_size", "maxsim_score_pq", "maxsim_score_i8",
+    "maxsim_score_varlen", "maxsim_score_pq_workspace_size", "maxsim_score_pq", "maxsim_score_pq_noalloc",
+    "maxsim_score_i8",
     "maxsim_backward_workspace_size", "maxsim_backward",
 )
 
@@ -80,6 +81,8 @@ def load_library():
     lib.maxsim_score_pq_workspace_size.argtypes = [I32, I32, I32]
     lib.maxsim_score_pq.restype = I32
     lib.maxsim_score_pq.argtypes = [P, I32, I32, P, I32, I32, P, P, I64, I64, P, P, P, SZ, P]
+    lib.maxsim_score_pq_noalloc.restype = I32
+    lib.maxsim_score_pq_noalloc.argtypes = [P, I32, I32, P, I32, I32, P, P, I64, I64, P, P, P]
     lib.maxsim_score_i8.restype = I32
     lib.maxsim_score_i8.argtypes = [P, P, I32, I32, P, P, P, I64, I64, P, P, P, P, P]
     lib.maxsim_backward_workspace_size.restype = SZ
@@ -207,6 +210,29 @@ def maxsim_score_pq(Q, codebooks, codes, offsets, out=None, argmax_out=None, wan
                              _ptr(out), _ptr(argmax_out), _ptr(workspace), workspace.numel(),
                              _stream(stream))
     _check(st, "maxsim_score_pq")
+    return (out, argmax_out) if argmax_out is not None else out
+
+
+def maxsim_score_pq_noalloc(Q, codebooks, codes, offsets, out=None, argmax_out=None, want_argmax=False,
+                            stream=None):
+    """PQ scoring with the table kept in the library's fixed device array, for
+    callers that cannot allocate device memory themselves (see the header)."""
+    lib = load_library()
+    _dev(Q, "Q", torch.float32)
+    _dev(codebooks, "codebooks", torch.float32)
+    _dev(codes, "codes", torch.uint8)
+    _dev(offsets, "offsets", torch.int64)
+    nq, d = Q.shape
+    M, K, _ = codebooks.shape
+    T = codes.shape[0]
+    B = offsets.numel() - 1
+    if out is None:
+        out = torch.empty(B, dtype=torch.float32, device=Q.device)
+    if want_argmax and argmax_out is None:
+        argmax_out = torch.empty((B, nq), dtype=torch.int32, device=Q.device)
+    st = lib.maxsim_score_pq_noalloc(_ptr(Q), nq, d, _ptr(codebooks), M, K, _ptr(codes), _ptr(offsets), B, T,
+                                     _ptr(out), _ptr(argmax_out), _stream(stream))
+    _check(st, "maxsim_score_pq_noalloc")
     return (out, argmax_out) if argmax_out is not None else out
 
 
