@@ -232,8 +232,13 @@ maxsim_status maxsim_score_i8(const int8_t *Q, const float *q_scale, int nq, int
  *   (rows no argmax points at are 0).
  *   workspace >= maxsim_backward_workspace_size(...) bytes (may be 0 -> NULL ok).
  *
- * Limits: d % 64 == 0, d <= 1024; n_queries * nq <= 65536; nd <= 65535.
- * An argmax entry outside [-1, L_b) is skipped and sets MAXSIM_DEVERR_BAD_INPUT.
+ * Limits: d % 64 == 0, d <= 1024; n_queries * nq <= 65536; the per-document
+ * sort must fit in shared memory: (9 * nd + n_queries * nq) * 4 bytes
+ * <= ~227 KB (e.g. nd <= 4096 with n_queries * nq = 16384). FP32 inputs
+ * return MAXSIM_ERR_UNSUPPORTED. An argmax entry outside [0, L_b) (or -1 for
+ * a non-empty document) is skipped and sets MAXSIM_DEVERR_BAD_INPUT.
+ * The workspace is unused (size query returns 0): the inverse CSR lives in
+ * shared memory, one document at a time.
  */
 size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd);
 maxsim_status maxsim_backward(const void *Q, int n_queries, int nq, int d,

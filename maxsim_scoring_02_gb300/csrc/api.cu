@@ -223,15 +223,32 @@ maxsim_status maxsim_score_i8(const int8_t* Q, const float* q_scale, int nq, int
 
 size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd) {
   (void)n_queries; (void)nq; (void)d; (void)B; (void)nd;
-  return 0;
+  return 0;  // the inverse CSR is built in shared memory, one document at a time
 }
 
 maxsim_status maxsim_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
                               const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
                               float* dQ, float* dD, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)Q; (void)n_queries; (void)nq; (void)d; (void)D; (void)B; (void)nd; (void)doc_len; (void)dtype;
-  (void)argmax; (void)dS; (void)dQ; (void)dD; (void)workspace; (void)workspace_bytes; (void)stream;
-  return MAXSIM_ERR_UNSUPPORTED;
+  (void)workspace;
+  (void)workspace_bytes;
+  if (n_queries < 1 || nq < 1 || d < 1 || B < 0 || nd < 1) return MAXSIM_ERR_INVALID_ARG;
+  if (dtype != MAXSIM_BF16 && dtype != MAXSIM_FP16) return dtype == MAXSIM_FP32 ? MAXSIM_ERR_UNSUPPORTED
+                                                                               : MAXSIM_ERR_INVALID_ARG;
+  if (d % 64 != 0 || d > 1024 || static_cast<int64_t>(n_queries) * nq > 65536 || nd > 65535)
+    return MAXSIM_ERR_UNSUPPORTED;
+  if (!Q || !dQ) return MAXSIM_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(dQ)) return MAXSIM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B == 0) {  // no documents: dQ is all zeros
+    return cudaMemsetAsync(dQ, 0, static_cast<size_t>(n_queries) * nq * d * sizeof(float), s) == cudaSuccess
+               ? MAXSIM_OK
+               : MAXSIM_ERR_CUDA;
+  }
+  if (!D || !argmax || !dS || !dD) return MAXSIM_ERR_INVALID_ARG;
+  if (!aligned16(D) || !aligned4(argmax) || !aligned4(dS) || !aligned16(dD) || (doc_len && !aligned4(doc_len)))
+    return MAXSIM_ERR_INVALID_ARG;
+  return launch_backward(Q, n_queries, nq, d, D, B, nd, doc_len, dtype == MAXSIM_BF16 ? 1 : 0, argmax, dS, dQ, dD,
+                         s);
 }
 
 }  // extern "C"

@@ -1,0 +1,311 @@
+// bwd.cu -- MaxSim backward through the saved forward argmax (FLASH-MAXSIM,
+// Abstract: the backward pass reuses the forward argmax, with an inverse-grid
+// CSR construction and an atomic-free, destination-owned reduction).
+//
+// With loss = sum_{q,b} dS[q,b] * score[q,b] and a = argmax[q,b,i]:
+//   dD[b,j,:] = sum_{(q,i) : a(q,b,i) = j} dS[q,b] * Q[q,i,:]     (dd_kernel)
+//   dQ[q,i,:] = sum_b dS[q,b] * D[b, a(q,b,i), :]                   (dq_kernel)
+//
+// dd_kernel -- one CTA per document (persistent over documents). The
+// document's nQ*nq argmax entries are grouped by token j with a counting
+// sort in shared memory: each warp counts its chunk of entries into a
+// private histogram (lanes holding the same key are found with
+// __match_any_sync and only their leader updates the warp's counter, so no
+// atomics are needed), a scan over (key, warp) gives the inverse CSR row
+// pointers, and a second pass scatters the entries stably. Then one warp per
+// destination row j sums dS * Q over its list in ascending entry order and
+// writes the row -- every row of dD[b] is written by exactly one warp, rows
+// nothing points at as zeros.
+//
+// dq_kernel -- each CTA owns a block of (q, i) destination rows with fp32
+// accumulators in registers and sweeps the documents in ascending order;
+// all CTAs sweep in the same order, so the gathered D rows of a document
+// are fetched from HBM once and re-served from L2.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace msim {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdWarps = kBwdThreads / 32;
+
+template <typename T>
+__device__ __forceinline__ float2 load2(const T* p);
+template <>
+__device__ __forceinline__ float2 load2<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+template <>
+__device__ __forceinline__ float2 load2<__half>(const __half* p) {
+  return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+
+struct BwdParams {
+  const void* Q;
+  const void* D;
+  const int32_t* doc_len;
+  const int32_t* argmax;
+  const float* dS;
+  float* dQ;
+  float* dD;
+  int64_t B;
+  int nQ, nq, d, nd;
+  unsigned* status;
+};
+
+__device__ __forceinline__ int doc_length(const BwdParams& p, int64_t b) {
+  if (!p.doc_len) return p.nd;
+  const int L = __ldg(p.doc_len + b);
+  return (L < 0 || L > p.nd) ? -1 : L;
+}
+
+// ------------------------------------------------------------------- dD
+// DPL = d / 32 values per lane (2 per bf16x2 load).
+template <typename T, int DPL>
+__global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
+  extern __shared__ int32_t bsm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nd = p.nd, ne = p.nQ * p.nq;
+  int32_t* counts = bsm;                       // [kBwdWarps][nd] -> offsets after the scan
+  int32_t* rowptr = counts + kBwdWarps * nd;   // [nd + 1]
+  int32_t* list = rowptr + nd + 1;             // [ne] sorted entry ids
+  float* dsv = reinterpret_cast<float*>(list + ne);   // [nQ]
+  int32_t* wsum = reinterpret_cast<int32_t*>(dsv + p.nQ);  // [kBwdWarps] scan scratch
+  const int chunk = (ne + kBwdWarps - 1) / kBwdWarps;
+  const int e_lo = warp * chunk, e_hi = min(ne, e_lo + chunk);
+  const T* Qp = static_cast<const T*>(p.Q);
+
+  for (int64_t b = blockIdx.x; b < p.B; b += gridDim.x) {
+    int L = doc_length(p, b);
+    if (L < 0) {
+      if (tid == 0) atomicOr(p.status, kDevErrBadInput);
+      L = 0;
+    }
+    for (int x = tid; x < kBwdWarps * nd; x += kBwdThreads) counts[x] = 0;
+    for (int q = tid; q < p.nQ; q += kBwdThreads) dsv[q] = __ldg(p.dS + static_cast<int64_t>(q) * p.B + b);
+    __syncthreads();
+    // pass 1: per-warp histograms of the argmax keys
+    bool bad = false;
+    for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
+      const int e = e0 + lane;
+      int key = -1;
+      if (e < e_hi) {
+        const int q = e / p.nq, i = e - q * p.nq;
+        key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
+        if (key < 0 || key >= L) {
+          if (!(key == -1 && L == 0)) bad = true;  // -1 is only valid for an empty document
+          key = -1;
+        }
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      if (key >= 0 && lane == __ffs(grp) - 1) counts[warp * nd + key] += __popc(grp);
+      __syncwarp();
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevErrBadInput);
+    __syncthreads();
+    // scan over (key, warp): offsets[w][j] = start[j] + sum_{w' < w} counts[w'][j]
+    {
+      const int per = (nd + kBwdThreads - 1) / kBwdThreads;
+      const int j0 = tid * per, j1 = min(nd, j0 + per);
+      int run = 0;
+      for (int j = j0; j < j1; ++j)
+        for (int w = 0; w < kBwdWarps; ++w) run += counts[w * nd + j];
+      // block-wide exclusive scan of the per-thread totals
+      int incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      int base = 0;
+      for (int w = 0; w < warp; ++w) base += wsum[w];
+      base += incl - run;
+      for (int j = j0; j < j1; ++j) {
+        rowptr[j] = base;
+        for (int w = 0; w < kBwdWarps; ++w) {
+          const int c = counts[w * nd + j];
+          counts[w * nd + j] = base;
+          base += c;
+        }
+      }
+      if (j1 == nd && j0 < j1) rowptr[nd] = base;
+    }
+    __syncthreads();
+    // pass 2: stable scatter of entry ids into the inverse CSR list
+    for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
+      const int e = e0 + lane;
+      int key = -1;
+      if (e < e_hi) {
+        const int q = e / p.nq, i = e - q * p.nq;
+        key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
+        if (key < 0 || key >= L) key = -1;
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      int pos = 0;
+      if (key >= 0) pos = counts[warp * nd + key] + __popc(grp & ((1u << lane) - 1u));
+      __syncwarp();
+      if (key >= 0) {
+        list[pos] = e;
+        if (lane == __ffs(grp) - 1) counts[warp * nd + key] += __popc(grp);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    // destination-owned rows: warp per row j of dD[b]
+    for (int j = warp; j < nd; j += kBwdWarps) {
+      float acc[DPL];
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+      const int r0 = rowptr[j], r1 = rowptr[j + 1];
+      for (int r = r0; r < r1; ++r) {
+        const int e = list[r];
+        const int q = e / p.nq;
+        const float g = dsv[q];
+        const T* qrow = Qp + static_cast<int64_t>(e) * p.d;   // Q[q, i, :] with e = q*nq + i
+#pragma unroll
+        for (int k = 0; k < DPL; k += 2) {
+          const float2 x = load2<T>(qrow + k * 32 + 2 * lane);
+          acc[k] = fmaf(g, x.x, acc[k]);
+          acc[k + 1] = fmaf(g, x.y, acc[k + 1]);
+        }
+      }
+      float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d);
+#pragma unroll
+      for (int k = 0; k < DPL; k += 2)
+        *reinterpret_cast<float2*>(drow + k * 32 + 2 * lane) = make_float2(acc[k], acc[k + 1]);
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------- dQ
+// Thread layout: TPR = d / 16 threads per destination row, 16 dims each.
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int rows_per_cta) {
+  const int tid = threadIdx.x;
+  const int tpr = p.d / 16;
+  const int rloc = tid / tpr, part = tid - rloc * tpr;
+  const int blocks_per_q = (p.nq + rows_per_cta - 1) / rows_per_cta;
+  const int q = blockIdx.x / blocks_per_q;
+  const int i = (blockIdx.x - q * blocks_per_q) * rows_per_cta + rloc;
+  const bool active = rloc < rows_per_cta && i < p.nq && q < p.nQ;
+  const T* Dp = static_cast<const T*>(p.D);
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  bool bad = false;
+  if (active) {
+    const int32_t* arow = p.argmax + static_cast<int64_t>(q) * p.B * p.nq + i;
+    const float* grow = p.dS + static_cast<int64_t>(q) * p.B;
+    constexpr int U = 4;  // documents in flight per thread
+    for (int64_t b0 = 0; b0 < p.B; b0 += U) {
+      int a[U];
+      float g[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t b = b0 + u;
+        a[u] = -1;
+        g[u] = 0.f;
+        if (b < p.B) {
+          a[u] = __ldg(arow + b * p.nq);
+          g[u] = __ldg(grow + b);
+          const int L = doc_length(p, b);
+          if (a[u] >= 0 && (L < 0 || a[u] >= L)) {
+            bad = true;
+            a[u] = -1;
+          } else if (a[u] < -1) {
+            bad = true;
+            a[u] = -1;
+          }
+        }
+      }
+      float x[U][16];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (a[u] >= 0) {
+          const T* row = Dp + ((b0 + u) * p.nd + a[u]) * static_cast<int64_t>(p.d) + part * 16;
+#pragma unroll
+          for (int k = 0; k < 16; k += 2) {
+            const float2 v = load2<T>(row + k);
+            x[u][k] = v.x;
+            x[u][k + 1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (a[u] >= 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) acc[k] = fmaf(g[u], x[u][k], acc[k]);
+        }
+    }
+    float* out = p.dQ + (static_cast<int64_t>(q) * p.nq + i) * p.d + part * 16;
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) *reinterpret_cast<float4*>(out + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
+  }
+  if (bad) atomicOr(p.status, kDevErrBadInput);
+}
+
+template <typename T>
+maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream_t stream) {
+  // dD
+  const size_t smem = (static_cast<size_t>(kBwdWarps) * p.nd + p.nd + 1 + static_cast<size_t>(p.nQ) * p.nq) * 4 +
+                      static_cast<size_t>(p.nQ) * 4 + kBwdWarps * 4;
+  if (smem > static_cast<size_t>(dev->max_smem_optin)) return MAXSIM_ERR_UNSUPPORTED;
+  const int64_t want = static_cast<int64_t>(dev->sm_count) * 2;
+  const int grid = static_cast<int>(p.B < want ? p.B : want);
+  cudaError_t e = cudaSuccess;
+  switch (p.d / 32) {
+#define MSIM_DD(DPL)                                                                                           \
+  case DPL:                                                                                                    \
+    e = cudaFuncSetAttribute(dd_kernel<T, DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+    if (e == cudaSuccess) dd_kernel<T, DPL><<<grid, kBwdThreads, smem, stream>>>(p);                           \
+    break;
+    MSIM_DD(2) MSIM_DD(4) MSIM_DD(6) MSIM_DD(8) MSIM_DD(10) MSIM_DD(12) MSIM_DD(14) MSIM_DD(16)
+    MSIM_DD(18) MSIM_DD(20) MSIM_DD(22) MSIM_DD(24) MSIM_DD(26) MSIM_DD(28) MSIM_DD(30) MSIM_DD(32)
+#undef MSIM_DD
+    default: return MAXSIM_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+  // dQ
+  const int tpr = p.d / 16;
+  const int rows = kBwdThreads / tpr;
+  const int blocks = p.nQ * ((p.nq + rows - 1) / rows);
+  dq_kernel<T><<<blocks, kBwdThreads, 0, stream>>>(p, rows);
+  return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+}  // namespace
+
+maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                              const int32_t* doc_len, int is_bf16, const int32_t* argmax, const float* dS, float* dQ,
+                              float* dD, cudaStream_t stream) {
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MAXSIM_ERR_CUDA;
+  BwdParams p;
+  p.Q = Q;
+  p.D = D;
+  p.doc_len = doc_len;
+  p.argmax = argmax;
+  p.dS = dS;
+  p.dQ = dQ;
+  p.dD = dD;
+  p.B = B;
+  p.nQ = n_queries;
+  p.nq = nq;
+  p.d = d;
+  p.nd = nd;
+  p.status = dev->status;
+  return is_bf16 ? launch_typed<__nv_bfloat16>(p, dev, stream) : launch_typed<__half>(p, dev, stream);
+}
+
+}  // namespace msim
