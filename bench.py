@@ -435,7 +435,22 @@ class ColPaliTrain:
         self.m.maxsim_score(self.Q, self.D, out=self.out, argmax_out=self.am)
         if ev is not None:
             ev[1].record()
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record()
         self.m.maxsim_backward(self.Q, self.D, self.am, self.dS, dQ=self.dQ, dD=self.dD)
+        if ev is not None:
+            b1.record()
+            self.bwd_events.append((b0, b1))
+
+    bwd_events = []
+
+    def extra(self):
+        """Backward (dD + dQ kernels) time and its HBM bytes: argmax read twice,
+        D rows gathered once from HBM (re-served from L2), dD written, dQ written."""
+        ms = sum(a.elapsed_time(b) for a, b in self.bwd_events) / max(1, len(self.bwd_events))
+        nbytes = (2 * 4.0 * self.nQ * self.B * self.nq + self.B * self.nd * self.d * 2 + 4.0 * self.B * self.nd * self.d
+                  + 4.0 * self.nQ * self.nq * self.d + 4.0 * self.nQ * self.B)
+        return {"backward_ms": ms, "backward_hbm_bytes": nbytes, "backward_gbs": nbytes / (ms / 1e3) / 1e9}
 
     def e2e_setup(self):
         self.h = [t.cpu().pin_memory() for t in (self.Q, self.D, self.dS)]
@@ -519,7 +534,7 @@ def rank_seed(rank):
 
 def cpu_baseline(wl, seconds):
     import oracle
-    fn, n = wl.cpu_sample(2000 if wl.nd * wl.d <= 128 * 128 else 500)
+    fn, n = wl.cpu_sample(2000 if getattr(wl, "nd", 128) * wl.d <= 128 * 128 else 500)
     cores = oracle.num_threads()
     fn()                                  # warm (page-in, thread pool)
     t0 = time.perf_counter()
@@ -694,6 +709,8 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
             "gpu_launches": wl.launches_per_step * args.steps,
         }
+        if hasattr(wl, "extra"):
+            line["extra"] = wl.extra()
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

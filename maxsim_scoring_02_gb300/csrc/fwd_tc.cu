@@ -17,22 +17,23 @@
 //    and walks it in groups of up to 256 chunks. The producer warp builds each
 //    group's slot table in shared memory (32 lanes load the document offsets
 //    in parallel), so no role waits on a global load in its issue loop.
-//  * Producer (warp 4, lane 0 issues): TMA loads of 64-dim x 32/128-row boxes,
+//  * Producer (warp 8, lane 0 issues): TMA loads of 64-dim x 32/128-row boxes,
 //    128-byte swizzled, into a ring of 16 KB stages; four contiguous slots go
 //    as one 128-row box. Every document byte is read from HBM once per
 //    (query, query chunk) pass -- with one query of up to 256 tokens that is
 //    the single pass of TileMaxSim §2(1) (BQ = Nq). With several queries or
 //    query chunks, all passes run over one group (<= 256 chunks) before the
 //    next, so the repeats are served by L2.
-//  * MMA (warp 5, lane 0 issues): tcgen05.mma kind::f16, M = 128 rows, N = NC
+//  * MMA (warp 9, lane 0 issues): tcgen05.mma kind::f16, M = 128 rows, N = NC
 //    query tokens, K = 16; every 64-wide d-slice of a tile accumulates into
 //    the same TMEM accumulator before any maximum is taken (TileMaxSim §2(2),
 //    dimension tiling). Up to four accumulators let it run ahead.
-//  * Slot partials (warps 0-3): tcgen05.ld of the warp's 32 lanes, rows past
+//  * Slot partials (warps 0-7, two groups of four taking tiles round-robin;
+//    warp w reads TMEM lane quarter w % 4): tcgen05.ld of 32 lanes, rows past
 //    the chunk's valid rows masked to -inf, a transpose butterfly of shuffles
 //    leaves lane l with the maximum (and lowest argmax) of query column l
 //    over the slot, handed over in a ring of shared-memory buffers.
-//  * Merge (warp 6): folds slot partials in document order and, when a
+//  * Merge (warp 10): folds slot partials in document order and, when a
 //    document ends, sums its per-token maxima and writes the score
 //    (FLASH-MAXSIM Figure 1: only the scalar score is written). Partial
 //    warps never wait for the merge except through the buffer ring. The
@@ -52,7 +53,11 @@
 namespace msim {
 namespace {
 
-constexpr int kThreads = 224;        // warps 0-3 slot partials, 4 producer, 5 MMA, 6 merge
+// Two groups of four slot-partial warps take tiles round-robin (warp w reads
+// TMEM lane quarter w % 4); then the producer, MMA and merge warps.
+constexpr int kGroups = 2;
+constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = 4 * kGroups + 1, kMergeWarp = 4 * kGroups + 2;
+constexpr int kThreads = 32 * (4 * kGroups + 3);
 constexpr int kStageBytes = 16384;   // 128 rows x 64 elements x 2 bytes
 constexpr int kSlotRows = 32;
 constexpr int kCapSlots = 256;       // chunk slots per group table
@@ -487,12 +492,13 @@ __device__ __forceinline__ void fin_push(int64_t (&fd)[kMaxFin], float (&fs)[kMa
 template <int NG, bool ARGMAX>
 __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
   constexpr int NC = 32 * NG;
-  const int tid = threadIdx.x;  // 0..127 == TMEM lane
-  const int warp = tid >> 5, lane = tid & 31;
-  const int A = p.n_acc, PB = p.n_part;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  int a = 0, pb = 0;
-  uint32_t aph = 0, pph = 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;            // slot index == TMEM lane quarter
+  const uint32_t grp = warp >> 2;          // groups take tiles round-robin
+  const int A = p.n_acc, PB = p.n_part;    // both powers of two
+  const int lgA = __ffs(A) - 1, lgPB = __ffs(PB) - 1;
+  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  uint32_t tt = 0;                         // global tile counter (same sequence as the MMA and merge)
   for (uint32_t gi = 0;; ++gi) {
     const int buf = gi & 1;
     if (!mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) return;
@@ -502,17 +508,22 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
     const int n_tiles = (n_slots + 3) >> 2;
     const int passes = p.n_queries * p.n_chunks;
     for (int pass = 0; pass < passes; ++pass) {
-      for (int t = 0; t < n_tiles; ++t) {
+      for (int t = 0; t < n_tiles; ++t, ++tt) {
+        if (tt % kGroups != grp) continue;
+        const int a = static_cast<int>(tt & static_cast<uint32_t>(A - 1));
+        const uint32_t aph = (tt >> lgA) & 1u;
+        const int pb = static_cast<int>(tt & static_cast<uint32_t>(PB - 1));
+        const uint32_t pph = (tt >> lgPB) & 1u;
         if (!mbar_wait_a(br.partempty + 8 * pb, pph ^ 1u, sm.abort_flag, p.status)) return;
         if (!mbar_wait_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
         tc_fence_after();
         const int i0 = 4 * t;
-        if (warp < n_slots - i0) {
-          const int info = T->slot_info[i0 + warp];
+        if (quarter < n_slots - i0) {
+          const int info = T->slot_info[i0 + quarter];
           const int vrows = info & 63;
           const int row = (info >> 6) * kSlotRows + lane;   // doc-local token index of this lane's row
-          float* pv = sm.part_v + (pb * 4 + warp) * NC;
-          int32_t* pi = sm.part_i + (pb * 4 + warp) * NC;
+          float* pv = sm.part_v + (pb * 4 + quarter) * NC;
+          int32_t* pi = sm.part_i + (pb * 4 + quarter) * NC;
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             float v[32];
@@ -537,15 +548,7 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
           __syncwarp();
           if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
         }
-        mbar_arrive_a(br.partfull + 8 * pb);  // every partial thread arrives (count 128)
-        if (++a == A) {
-          a = 0;
-          aph ^= 1u;
-        }
-        if (++pb == PB) {
-          pb = 0;
-          pph ^= 1u;
-        }
+        mbar_arrive_a(br.partfull + 8 * pb);  // every thread of the group arrives (count 128)
       }
     }
     __syncwarp();
@@ -712,22 +715,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* rest = sm.bars + 2 * p.stages;
     for (int i = 0; i < 4; ++i) mbar_init(rest + i, 1);                    // qfull[2], qempty[2]
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + i, 1);          // accfull
-    for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + p.n_acc + i, 4);  // accempty: one per epilogue warp
+    for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + p.n_acc + i, 4);  // accempty: the 4 warps of one group
     for (int i = 0; i < 2; ++i) mbar_init(rest + 4 + 2 * p.n_acc + i, 1);  // tabfull
-    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 6);  // tabempty: MMA + 4 partial + merge
+    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 4 * kGroups + 2);  // tabempty: MMA + partials + merge
     uint64_t* pr = rest + 8 + 2 * p.n_acc;
-    for (int i = 0; i < p.n_part; ++i) mbar_init(pr + i, 128);             // partfull: every partial thread
+    for (int i = 0; i < p.n_part; ++i) mbar_init(pr + i, 128);             // partfull: the threads of one group
     for (int i = 0; i < p.n_part; ++i) mbar_init(pr + p.n_part + i, 1);    // partempty: merge warp
     mbar_init(pr + 2 * p.n_part, 1);                                       // done
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tm_d128);
     tma_prefetch_desc(&tm_d32);
     tma_prefetch_desc(&tm_q);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sm.tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
@@ -739,11 +742,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t b0 = (p.B * blockIdx.x) / gridDim.x;
   const int64_t b1 = (p.B * (blockIdx.x + 1)) / gridDim.x;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     run_producer<NC>(p, sm, br, &tm_d128, &tm_d32, &tm_q, b0, b1);
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) run_mma<NC>(p, sm, br, tmem_base);
-  } else if (warp == 6) {
+  } else if (warp == kMergeWarp) {
     run_merge<NG, ARGMAX>(p, sm, br);
   } else {
     run_partials<NG, ARGMAX>(p, sm, br, tmem_base);
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
@@ -799,7 +802,7 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   const size_t budget = static_cast<size_t>(dev->max_smem_optin);
   const int n_part = NC >= 128 ? 2 : 4;
   int n_qslots = 1;
-  if (multipass && smem_bytes_for(NC, KB, 6, n_acc, 2, n_part) <= budget) n_qslots = 2;
+  if (multipass && smem_bytes_for(NC, KB, 4, n_acc, 2, n_part) <= budget) n_qslots = 2;
   int stages = 16;
   while (stages > 2 && smem_bytes_for(NC, KB, stages, n_acc, n_qslots, n_part) > budget) --stages;
   const size_t smem = smem_bytes_for(NC, KB, stages, n_acc, n_qslots, n_part);
