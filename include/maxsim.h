@@ -144,8 +144,9 @@ maxsim_status maxsim_score_varlen(const void *Q, int n_queries, int nq, int d,
  *              contents on entry are ignored, the call overwrites it.
  *
  * Limits: 1 <= nq <= 1024; M % 4 == 0, 4 <= M <= 64; 1 <= K <= 256;
- * d % M == 0, d <= 1024; M * K * 32 bytes (one 8-token table group) must fit
- * in shared memory (M * K <= 7168). A code >= K is clamped to K-1 and sets
+ * d % M == 0, d <= 1024; one 8-token table group (M * K * 32 bytes) plus
+ * 64 KB of code staging must fit in shared memory (M * K <= 5056), else
+ * MAXSIM_ERR_UNSUPPORTED. A code >= K is clamped to K-1 and sets
  * MAXSIM_DEVERR_BAD_INPUT. Missing or short workspace: MAXSIM_ERR_WORKSPACE.
  */
 size_t maxsim_score_pq_workspace_size(int nq, int M, int K);
@@ -233,8 +234,8 @@ maxsim_status maxsim_score_i8(const int8_t *Q, const float *q_scale, int nq, int
  *   workspace >= maxsim_backward_workspace_size(...) bytes (may be 0 -> NULL ok).
  *
  * Limits: d % 64 == 0, d <= 1024; n_queries * nq <= 65536; the per-document
- * sort must fit in shared memory: (9 * nd + n_queries * nq) * 4 bytes
- * <= ~227 KB (e.g. nd <= 4096 with n_queries * nq = 16384). FP32 inputs
+ * sort must fit in shared memory: about (10 * nd + 2 * n_queries * nq) * 2
+ * bytes <= ~227 KB (e.g. nd <= 8192 with n_queries * nq = 16384). FP32 inputs
  * return MAXSIM_ERR_UNSUPPORTED. An argmax entry outside [0, L_b) (or -1 for
  * a non-empty document) is skipped and sets MAXSIM_DEVERR_BAD_INPUT.
  * The workspace is unused (size query returns 0): the inverse CSR lives in

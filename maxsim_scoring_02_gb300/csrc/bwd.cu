@@ -73,11 +73,13 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
   extern __shared__ int32_t bsm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nd = p.nd, ne = p.nQ * p.nq;
-  int32_t* counts = bsm;                       // [kBwdWarps][nd] -> offsets after the scan
-  int32_t* rowptr = counts + kBwdWarps * nd;   // [nd + 1]
-  int32_t* list = rowptr + nd + 1;             // [ne] sorted entry ids
-  float* dsv = reinterpret_cast<float*>(list + ne);   // [nQ]
-  int32_t* wsum = reinterpret_cast<int32_t*>(dsv + p.nQ);  // [kBwdWarps] scan scratch
+  // 16-bit storage: tokens < 65535, entries and positions < 65536
+  int32_t* rowptr = bsm;                                                   // [nd + 1]
+  float* dsv = reinterpret_cast<float*>(rowptr + nd + 1);                  // [nQ]
+  int32_t* wsum = reinterpret_cast<int32_t*>(dsv + p.nQ);                  // [kBwdWarps] scan scratch
+  uint16_t* counts = reinterpret_cast<uint16_t*>(wsum + kBwdWarps);        // [kBwdWarps][nd] -> offsets
+  uint16_t* list = counts + kBwdWarps * nd;                                // [ne] sorted entry ids
+  uint16_t* keys = list + ne;                                              // [ne] token + 1 (0 = skip)
   const int chunk = (ne + kBwdWarps - 1) / kBwdWarps;
   const int e_lo = warp * chunk, e_hi = min(ne, e_lo + chunk);
   const T* Qp = static_cast<const T*>(p.Q);
@@ -90,25 +92,30 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
     }
     for (int x = tid; x < kBwdWarps * nd; x += kBwdThreads) counts[x] = 0;
     for (int q = tid; q < p.nQ; q += kBwdThreads) dsv[q] = __ldg(p.dS + static_cast<int64_t>(q) * p.B + b);
-    __syncthreads();
-    // pass 1: per-warp histograms of the argmax keys
+    // stage the document's argmax entries (coalesced per query row), validated:
+    // -1 is only valid for an empty document; anything outside [0, L) is skipped
     bool bad = false;
-    for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
-      const int e = e0 + lane;
-      int key = -1;
-      if (e < e_hi) {
-        const int q = e / p.nq, i = e - q * p.nq;
-        key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
-        if (key < 0 || key >= L) {
-          if (!(key == -1 && L == 0)) bad = true;  // -1 is only valid for an empty document
-          key = -1;
-        }
+#pragma unroll 8
+    for (int e = tid; e < ne; e += kBwdThreads) {
+      const int q = e / p.nq, i = e - q * p.nq;
+      int key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
+      if (key < 0 || key >= L) {
+        if (!(key == -1 && L == 0)) bad = true;
+        key = -1;
       }
-      const unsigned grp = __match_any_sync(0xffffffffu, key);
-      if (key >= 0 && lane == __ffs(grp) - 1) counts[warp * nd + key] += __popc(grp);
-      __syncwarp();
+      keys[e] = static_cast<uint16_t>(key + 1);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevErrBadInput);
+    __syncthreads();
+    // pass 1: per-warp histograms of the argmax keys
+    for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
+      const int e = e0 + lane;
+      const int key = e < e_hi ? static_cast<int>(keys[e]) - 1 : -1;
+      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      if (key >= 0 && lane == __ffs(grp) - 1)
+        counts[warp * nd + key] = static_cast<uint16_t>(counts[warp * nd + key] + __popc(grp));
+      __syncwarp();
+    }
     __syncthreads();
     // scan over (key, warp): offsets[w][j] = start[j] + sum_{w' < w} counts[w'][j]
     {
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
         rowptr[j] = base;
         for (int w = 0; w < kBwdWarps; ++w) {
           const int c = counts[w * nd + j];
-          counts[w * nd + j] = base;
+          counts[w * nd + j] = static_cast<uint16_t>(base);
           base += c;
         }
       }
@@ -143,19 +150,14 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
     // pass 2: stable scatter of entry ids into the inverse CSR list
     for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
       const int e = e0 + lane;
-      int key = -1;
-      if (e < e_hi) {
-        const int q = e / p.nq, i = e - q * p.nq;
-        key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
-        if (key < 0 || key >= L) key = -1;
-      }
+      const int key = e < e_hi ? static_cast<int>(keys[e]) - 1 : -1;
       const unsigned grp = __match_any_sync(0xffffffffu, key);
       int pos = 0;
       if (key >= 0) pos = counts[warp * nd + key] + __popc(grp & ((1u << lane) - 1u));
       __syncwarp();
       if (key >= 0) {
-        list[pos] = e;
-        if (lane == __ffs(grp) - 1) counts[warp * nd + key] += __popc(grp);
+        list[pos] = static_cast<uint16_t>(e);
+        if (lane == __ffs(grp) - 1) counts[warp * nd + key] = static_cast<uint16_t>(counts[warp * nd + key] + __popc(grp));
       }
       __syncwarp();
     }
@@ -166,17 +168,30 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
 #pragma unroll
       for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
       const int r0 = rowptr[j], r1 = rowptr[j + 1];
-      for (int r = r0; r < r1; ++r) {
-        const int e = list[r];
-        const int q = e / p.nq;
-        const float g = dsv[q];
-        const T* qrow = Qp + static_cast<int64_t>(e) * p.d;   // Q[q, i, :] with e = q*nq + i
+      // gathers of up to 4 entries are issued together; the FMAs stay in entry order
+      for (int r = r0; r < r1; r += 4) {
+        float2 x[4][DPL / 2];
+        float gq[4];
 #pragma unroll
-        for (int k = 0; k < DPL; k += 2) {
-          const float2 x = load2<T>(qrow + k * 32 + 2 * lane);
-          acc[k] = fmaf(g, x.x, acc[k]);
-          acc[k + 1] = fmaf(g, x.y, acc[k + 1]);
+        for (int u = 0; u < 4; ++u) {
+          gq[u] = 0.f;
+          if (r + u < r1) {
+            const int e = list[r + u];
+            gq[u] = dsv[e / p.nq];
+            const T* qrow = Qp + static_cast<int64_t>(e) * p.d;   // Q[q, i, :] with e = q*nq + i
+#pragma unroll
+            for (int k = 0; k < DPL; k += 2) x[u][k / 2] = load2<T>(qrow + k * 32 + 2 * lane);
+          }
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (r + u < r1) {
+#pragma unroll
+            for (int k = 0; k < DPL; k += 2) {
+              acc[k] = fmaf(gq[u], x[u][k / 2].x, acc[k]);
+              acc[k + 1] = fmaf(gq[u], x[u][k / 2].y, acc[k + 1]);
+            }
+          }
       }
       float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d);
 #pragma unroll
@@ -258,8 +273,8 @@ __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int 
 template <typename T>
 maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream_t stream) {
   // dD
-  const size_t smem = (static_cast<size_t>(kBwdWarps) * p.nd + p.nd + 1 + static_cast<size_t>(p.nQ) * p.nq) * 4 +
-                      static_cast<size_t>(p.nQ) * 4 + kBwdWarps * 4;
+  const size_t smem = (static_cast<size_t>(p.nd) + 1 + p.nQ + kBwdWarps) * 4 +
+                      (static_cast<size_t>(kBwdWarps) * p.nd + 2 * static_cast<size_t>(p.nQ) * p.nq) * 2;
   if (smem > static_cast<size_t>(dev->max_smem_optin)) return MAXSIM_ERR_UNSUPPORTED;
   const int64_t want = static_cast<int64_t>(dev->sm_count) * 2;
   const int grid = static_cast<int>(p.B < want ? p.B : want);

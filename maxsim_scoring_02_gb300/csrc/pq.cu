@@ -16,8 +16,11 @@
 //
 // Scoring thread map: a warp owns one document at a time; lane = (token
 // slot tk = lane/8, query token i = lane%8), so the 8 lanes of a token read
-// 32 consecutive bytes of the table per subspace. Lowest token index wins
-// ties, as in the other paths.
+// 32 consecutive bytes of the table per subspace. A warp walks its
+// documents as pieces of <= 2 KB of codes, staged into a per-warp double
+// buffer in shared memory with cp.async, so the next piece is in flight
+// while the current one is scored; document offsets come 32 at a time.
+// Lowest token index wins ties, as in the other paths.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -29,7 +32,7 @@
 namespace msim {
 namespace {
 
-constexpr int kPqThreads = 256;
+constexpr int kPqThreads = 512;
 constexpr int kGroup = 8;  // query tokens per table group
 
 __global__ void pq_table_kernel(const float* __restrict__ Q, int nq, int d, const float* __restrict__ C, int M,
@@ -64,7 +67,71 @@ struct PqParams {
   unsigned* status;
 };
 
-// Codes of one token as 32-bit words (M % 4 == 0); word w holds subspaces 4w..4w+3.
+constexpr int kPieceBytes = 2048;   // codes staged per warp per piece (double-buffered)
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// A piece: up to kPieceBytes / M consecutive tokens of one document.
+struct Piece {
+  int64_t b;      // document (-1: none)
+  int64_t row0;   // first token row in codes
+  int j0;         // doc-local index of the first token
+  int n;          // tokens in the piece (0 for an empty or rejected document)
+  bool last;      // the document's last piece
+};
+
+// Per-warp walk over documents b_first, b_first + stride, ... < b_end, with
+// offsets fetched 32 documents at a time into registers (lane k holds doc k).
+struct DocWalk {
+  int64_t b_first, b_end, stride;
+  int64_t kbase;         // index k of the documents currently held in registers
+  int64_t s_reg, e_reg;  // this lane's document (k = kbase + lane)
+  int cap;               // tokens per piece
+  unsigned* status;
+  const int64_t* offsets;
+  int64_t total;
+
+  __device__ __forceinline__ void load(int64_t k0) {
+    kbase = k0;
+    const int lane = threadIdx.x & 31;
+    const int64_t b = b_first + (k0 + lane) * stride;
+    s_reg = e_reg = 0;
+    if (b < b_end) {
+      s_reg = __ldg(offsets + b);
+      e_reg = __ldg(offsets + b + 1);
+    }
+  }
+  // First piece of document index k (k-th document of this warp).
+  __device__ __forceinline__ Piece doc_piece(int64_t k, int j0) {
+    Piece pc;
+    pc.b = b_first + k * stride;
+    if (pc.b >= b_end) {
+      pc.b = -1;
+      return pc;
+    }
+    if (k - kbase >= 32) load(k);
+    const int src = static_cast<int>(k - kbase);
+    const int64_t s0 = __shfl_sync(0xffffffffu, s_reg, src), e0 = __shfl_sync(0xffffffffu, e_reg, src);
+    const bool bad = s0 < 0 || e0 < s0 || e0 > total || e0 - s0 > INT_MAX;
+    if (bad && j0 == 0 && (threadIdx.x & 31) == 0) atomicOr(status, kDevErrBadInput);
+    const int64_t L = bad ? 0 : e0 - s0;
+    pc.row0 = s0 + j0;
+    pc.j0 = j0;
+    const int64_t left = L - j0;
+    pc.n = static_cast<int>(left < cap ? (left > 0 ? left : 0) : cap);
+    pc.last = j0 + pc.n >= L;
+    return pc;
+  }
+};
+
 template <bool ARGMAX>
 __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams p) {
   extern __shared__ float4 pq_smem4[];
@@ -74,8 +141,12 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
   const int M = p.M, K = p.K, MW = M >> 2;
   const uint32_t kmax = static_cast<uint32_t>(K - 1);
   const int64_t b0 = (p.B * blockIdx.x) / gridDim.x, b1 = (p.B * (blockIdx.x + 1)) / gridDim.x;
-  const int64_t tsize = static_cast<int64_t>(M) * K * kGroup;  // floats per group
-  const uint32_t* codes32 = reinterpret_cast<const uint32_t*>(p.codes);
+  const int64_t tsize = static_cast<int64_t>(M) * K * kGroup;  // floats per table group
+  uint32_t* stage = reinterpret_cast<uint32_t*>(Ts + tsize) + warp * (2 * kPieceBytes / 4);
+  const uint32_t stage_s = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+  const int cap = kPieceBytes / M;
+  // 16-byte copies need 16-byte rows and a 16-byte aligned codes base
+  const bool vec16 = (M & 15) == 0 && (reinterpret_cast<uintptr_t>(p.codes) & 15) == 0;
 
   for (int g = 0; g < p.n_groups; ++g) {
     __syncthreads();
@@ -83,63 +154,97 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
     for (int64_t e = tid; e < tsize / 4; e += kPqThreads) pq_smem4[e] = __ldg(src + e);
     __syncthreads();
     const int qi = g * kGroup + ii;
-    for (int64_t b = b0 + warp; b < b1; b += kPqThreads / 32) {
-      const int64_t s0 = __ldg(p.offsets + b), e0 = __ldg(p.offsets + b + 1);
-      const bool bad = s0 < 0 || e0 < s0 || e0 > p.total_tokens;
-      if (bad && g == 0 && lane == 0) atomicOr(p.status, kDevErrBadInput);
-      const int64_t L = bad ? 0 : e0 - s0;
-      float rm = -INFINITY;
-      int ra = INT_MAX;
-      bool badc = false;
-      // token j = 4*it + tk; codes of the next iteration are loaded before the current one is scored
-      uint32_t cw[16], nw[16];
-      const uint32_t* row = codes32 + (s0 + tk) * MW;
-#pragma unroll
-      for (int w = 0; w < 16; ++w)
-        if (w < MW) cw[w] = (tk < L) ? __ldg(row + w) : 0u;
-      for (int64_t j = tk; j < L; j += 4) {
-        const int64_t jn = j + 4;
-#pragma unroll
-        for (int w = 0; w < 16; ++w)
-          if (w < MW) nw[w] = (jn < L) ? __ldg(row + (jn - tk) * MW + w) : 0u;
+
+    DocWalk walk;
+    walk.b_first = b0 + warp;
+    walk.b_end = b1;
+    walk.stride = kPqThreads / 32;
+    walk.cap = cap;
+    walk.status = p.status;
+    walk.offsets = p.offsets;
+    walk.total = p.total_tokens;
+    walk.load(0);
+
+    // stage the codes of a piece into buffer `bufi` of this warp
+    auto issue = [&](const Piece& pc, int bufi) {
+      const uint32_t dst = stage_s + static_cast<uint32_t>(bufi * kPieceBytes);
+      const uint8_t* srcb = p.codes + pc.row0 * M;
+      const int bytes = pc.n * M;
+      if (vec16) {
+        for (int o = lane * 16; o < bytes; o += 512) cp_async16(dst + o, srcb + o);
+      } else {
+        for (int o = lane * 4; o < bytes; o += 128) cp_async4(dst + o, srcb + o);
+      }
+      cp_async_commit();
+    };
+
+    int64_t k = 0;
+    Piece cur = walk.doc_piece(0, 0);
+    int bufi = 0;
+    if (cur.b >= 0) issue(cur, 0);
+    float rm = -INFINITY;
+    int ra = INT_MAX;
+    bool badc = false;
+    while (cur.b >= 0) {
+      // the next piece: rest of this document, or the next document
+      Piece nxt;
+      if (!cur.last) {
+        nxt = walk.doc_piece(k, cur.j0 + cur.n);
+      } else {
+        nxt = walk.doc_piece(k + 1, 0);
+      }
+      if (nxt.b >= 0) {
+        issue(nxt, bufi ^ 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncwarp();
+      // score the staged piece: token t = 4*it + tk
+      const uint32_t* cw_base = stage + bufi * (kPieceBytes / 4);
+      for (int t = tk; t < cur.n; t += 4) {
         float s = 0.f;
+        for (int w = 0; w < MW; ++w) {
+          const uint32_t word = cw_base[t * MW + w];
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          if (w < MW) {
-#pragma unroll
-            for (int sb = 0; sb < 4; ++sb) {
-              const int m = 4 * w + sb;
-              const uint32_t raw = (cw[w] >> (8 * sb)) & 0xFFu;
-              badc |= raw > kmax;                       // a code outside the codebook is clamped and reported
-              s += Ts[(m * K + static_cast<int>(min(raw, kmax))) * kGroup + ii];
-            }
+          for (int sb = 0; sb < 4; ++sb) {
+            const int m = 4 * w + sb;
+            const uint32_t raw = (word >> (8 * sb)) & 0xFFu;
+            badc |= raw > kmax;  // a code outside the codebook is clamped and reported
+            s += Ts[(m * K + static_cast<int>(min(raw, kmax))) * kGroup + ii];
           }
         }
         if (s > rm) {  // tokens ascend per lane: strict > keeps the lowest index
           rm = s;
-          ra = static_cast<int>(j);
-        }
-#pragma unroll
-        for (int w = 0; w < 16; ++w)
-          if (w < MW) cw[w] = nw[w];
-      }
-      if (__any_sync(0xffffffffu, badc) && lane == 0 && g == 0) atomicOr(p.status, kDevErrBadInput);
-      // max over the 4 token slots (lanes ii, ii+8, ii+16, ii+24)
-#pragma unroll
-      for (int o = 8; o <= 16; o <<= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, rm, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, ra, o);
-        if (v2 > rm || (v2 == rm && i2 < ra)) {
-          rm = v2;
-          ra = i2;
+          ra = cur.j0 + t;
         }
       }
-      float part = (L > 0 && qi < p.nq) ? rm : 0.f;
-      if (ARGMAX && tk == 0 && qi < p.nq) p.argmax[b * p.nq + qi] = L > 0 ? ra : -1;
+      __syncwarp();  // the buffer is refilled two pieces later
+      if (cur.last) {
+        // max over the 4 token slots (lanes ii, ii+8, ii+16, ii+24)
 #pragma unroll
-      for (int o = 1; o <= 4; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (lane == 0) p.out[b] = (g == 0 ? 0.f : p.out[b]) + part;
+        for (int o = 8; o <= 16; o <<= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, rm, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, ra, o);
+          if (v2 > rm || (v2 == rm && i2 < ra)) {
+            rm = v2;
+            ra = i2;
+          }
+        }
+        const bool nonempty = cur.j0 + cur.n > 0;
+        float part = (nonempty && qi < p.nq) ? rm : 0.f;
+        if (ARGMAX && tk == 0 && qi < p.nq) p.argmax[cur.b * p.nq + qi] = nonempty ? ra : -1;
+#pragma unroll
+        for (int o = 1; o <= 4; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) p.out[cur.b] = (g == 0 ? 0.f : p.out[cur.b]) + part;
+        rm = -INFINITY;
+        ra = INT_MAX;
+        ++k;
+      }
+      cur = nxt;
+      bufi ^= 1;
     }
+    if (__any_sync(0xffffffffu, badc) && lane == 0 && g == 0) atomicOr(p.status, kDevErrBadInput);
   }
 }
 
@@ -155,7 +260,8 @@ maxsim_status launch_pq(const float* Q, int nq, int d, const float* C, int M, in
                         float* table, cudaStream_t stream) {
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(M) * K * kGroup * sizeof(float);
+  const size_t smem = static_cast<size_t>(M) * K * kGroup * sizeof(float) +
+                      static_cast<size_t>(kPqThreads / 32) * 2 * kPieceBytes;
   if (smem > static_cast<size_t>(dev->max_smem_optin)) return MAXSIM_ERR_UNSUPPORTED;
   const int n_groups = (nq + kGroup - 1) / kGroup;
   {

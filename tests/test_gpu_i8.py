@@ -108,3 +108,15 @@ def test_i8_many_docs_sampled():
                                               sd.numpy()[offn[b]:offn[b + 1]], o2)
         assert (md[b].cpu().numpy() == rmd[0]).all() and (am[b].cpu().numpy() == ram[0]).all()
         assert (mv[b].cpu().numpy() == rmv[0]).all()
+
+
+def test_bad_offsets_are_reported_not_faulted():
+    """Offsets beyond the packed rows: the kernel's own checks score those
+    documents as empty and set the bad-input bit."""
+    Qi, sq, Di, sd, _ = _inputs(4, 32, 128, seed=221)
+    off = torch.tensor([0, 5, 3, 10_000_000, int(Di.shape[0])], dtype=torch.int64)
+    out, mv, md, am = m.maxsim_score_i8(Qi.to(DEV), sq.to(DEV), Di.to(DEV), sd.to(DEV), off.to(DEV),
+                                        want_details=True)
+    st, flags = m.maxsim_device_status()
+    assert st == 1 and flags & m.DEVERR_BAD_INPUT
+    assert out[1].item() == 0.0 and (am[1] == -1).all() and out[2].item() == 0.0
