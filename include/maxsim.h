@@ -231,15 +231,19 @@ maxsim_status maxsim_score_i8(const int8_t *Q, const float *q_scale, int nq, int
  *   (-1 = empty document); dS [n_queries, B] fp32.
  *   dQ [n_queries, nq, d] fp32 and dD [B, nd, d] fp32 are fully written
  *   (rows no argmax points at are 0).
- *   workspace >= maxsim_backward_workspace_size(...) bytes (may be 0 -> NULL ok).
+ *   workspace >= maxsim_backward_workspace_size(...) bytes (see below).
  *
  * Limits: d % 64 == 0, d <= 1024; n_queries * nq <= 65536; the per-document
  * sort must fit in shared memory: about (10 * nd + 2 * n_queries * nq) * 2
  * bytes <= ~227 KB (e.g. nd <= 8192 with n_queries * nq = 16384). FP32 inputs
  * return MAXSIM_ERR_UNSUPPORTED. An argmax entry outside [0, L_b) (or -1 for
  * a non-empty document) is skipped and sets MAXSIM_DEVERR_BAD_INPUT.
- * The workspace is unused (size query returns 0): the inverse CSR lives in
- * shared memory, one document at a time.
+ * The inverse CSR lives in shared memory, one document at a time. For
+ * B >= 2048 the dQ sweep is split into up to 8 document ranges whose
+ * partial sums go to the workspace (maxsim_backward_workspace_size bytes,
+ * 16-byte aligned; 0 bytes -- NULL allowed -- for smaller B) and are added
+ * in range order, so results do not depend on scheduling. A missing or
+ * short workspace returns MAXSIM_ERR_WORKSPACE.
  */
 size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd);
 maxsim_status maxsim_backward(const void *Q, int n_queries, int nq, int d,

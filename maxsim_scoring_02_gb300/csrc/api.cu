@@ -222,15 +222,14 @@ maxsim_status maxsim_score_i8(const int8_t* Q, const float* q_scale, int nq, int
 }
 
 size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, int nd) {
-  (void)n_queries; (void)nq; (void)d; (void)B; (void)nd;
-  return 0;  // the inverse CSR is built in shared memory, one document at a time
+  (void)nd;  // the inverse CSR is built in shared memory, one document at a time
+  if (n_queries < 1 || nq < 1 || d < 1 || B < 0) return 0;
+  return backward_workspace_bytes(n_queries, nq, d, B);  // per-range dQ partials
 }
 
 maxsim_status maxsim_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
                               const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
                               float* dQ, float* dD, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (n_queries < 1 || nq < 1 || d < 1 || B < 0 || nd < 1) return MAXSIM_ERR_INVALID_ARG;
   if (dtype != MAXSIM_BF16 && dtype != MAXSIM_FP16) return dtype == MAXSIM_FP32 ? MAXSIM_ERR_UNSUPPORTED
                                                                                : MAXSIM_ERR_INVALID_ARG;
@@ -247,8 +246,10 @@ maxsim_status maxsim_backward(const void* Q, int n_queries, int nq, int d, const
   if (!D || !argmax || !dS || !dD) return MAXSIM_ERR_INVALID_ARG;
   if (!aligned16(D) || !aligned4(argmax) || !aligned4(dS) || !aligned16(dD) || (doc_len && !aligned4(doc_len)))
     return MAXSIM_ERR_INVALID_ARG;
+  const size_t need = backward_workspace_bytes(n_queries, nq, d, B);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return MAXSIM_ERR_WORKSPACE;
   return launch_backward(Q, n_queries, nq, d, D, B, nd, doc_len, dtype == MAXSIM_BF16 ? 1 : 0, argmax, dS, dQ, dD,
-                         s);
+                         static_cast<float*>(workspace), s);
 }
 
 }  // extern "C"

@@ -18,9 +18,11 @@
 // nothing points at as zeros.
 //
 // dq_kernel -- each CTA owns a block of (q, i) destination rows with fp32
-// accumulators in registers and sweeps the documents in ascending order;
-// all CTAs sweep in the same order, so the gathered D rows of a document
-// are fetched from HBM once and re-served from L2.
+// accumulators in registers and sweeps one contiguous range of documents in
+// ascending order; the CTAs of a range sweep in the same order, so the
+// gathered D rows are re-served from L2. With several ranges each writes its
+// own partial dQ to the workspace and dq_reduce_kernel adds them in range
+// order -- still destination-owned, atomic-free and deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -57,6 +59,9 @@ struct BwdParams {
   float* dD;
   int64_t B;
   int nQ, nq, d, nd;
+  int nq_shift;      // log2(nq) when nq is a power of two, else -1
+  int splits;        // dQ document ranges (partials summed in range order)
+  float* partial;    // [splits][nQ][nq][d] workspace (splits > 1)
   unsigned* status;
 };
 
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
           gq[u] = 0.f;
           if (r + u < r1) {
             const int e = list[r + u];
-            gq[u] = dsv[e / p.nq];
+            gq[u] = dsv[p.nq_shift >= 0 ? (e >> p.nq_shift) : (e / p.nq)];
             const T* qrow = Qp + static_cast<int64_t>(e) * p.d;   // Q[q, i, :] with e = q*nq + i
 #pragma unroll
             for (int k = 0; k < DPL; k += 2) x[u][k / 2] = load2<T>(qrow + k * 32 + 2 * lane);
@@ -203,26 +208,29 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
 }
 
 // ------------------------------------------------------------------- dQ
-// Thread layout: TPR = d / 16 threads per destination row, 16 dims each.
+// Thread layout: d / 8 threads per destination row, 8 dims each; blockIdx.y
+// picks one of `splits` contiguous document ranges. With one range the sum
+// goes straight to dQ, otherwise to partial[range] for dq_reduce_kernel.
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int rows_per_cta) {
   const int tid = threadIdx.x;
-  const int tpr = p.d / 16;
+  const int tpr = p.d / 8;
   const int rloc = tid / tpr, part = tid - rloc * tpr;
   const int blocks_per_q = (p.nq + rows_per_cta - 1) / rows_per_cta;
   const int q = blockIdx.x / blocks_per_q;
   const int i = (blockIdx.x - q * blocks_per_q) * rows_per_cta + rloc;
   const bool active = rloc < rows_per_cta && i < p.nq && q < p.nQ;
+  const int64_t bs = (p.B * blockIdx.y) / p.splits, be = (p.B * (blockIdx.y + 1)) / p.splits;
   const T* Dp = static_cast<const T*>(p.D);
-  float acc[16];
+  float acc[8];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
   bool bad = false;
   if (active) {
     const int32_t* arow = p.argmax + static_cast<int64_t>(q) * p.B * p.nq + i;
     const float* grow = p.dS + static_cast<int64_t>(q) * p.B;
-    constexpr int U = 4;  // documents in flight per thread
-    for (int64_t b0 = 0; b0 < p.B; b0 += U) {
+    constexpr int U = 8;  // documents in flight per thread
+    for (int64_t b0 = bs; b0 < be; b0 += U) {
       int a[U];
       float g[U];
 #pragma unroll
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int 
         const int64_t b = b0 + u;
         a[u] = -1;
         g[u] = 0.f;
-        if (b < p.B) {
+        if (b < be) {
           a[u] = __ldg(arow + b * p.nq);
           g[u] = __ldg(grow + b);
           const int L = doc_length(p, b);
@@ -243,13 +251,13 @@ __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int 
           }
         }
       }
-      float x[U][16];
+      float x[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (a[u] >= 0) {
-          const T* row = Dp + ((b0 + u) * p.nd + a[u]) * static_cast<int64_t>(p.d) + part * 16;
+          const T* row = Dp + ((b0 + u) * p.nd + a[u]) * static_cast<int64_t>(p.d) + part * 8;
 #pragma unroll
-          for (int k = 0; k < 16; k += 2) {
+          for (int k = 0; k < 8; k += 2) {
             const float2 v = load2<T>(row + k);
             x[u][k] = v.x;
             x[u][k + 1] = v.y;
@@ -260,14 +268,34 @@ __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int 
       for (int u = 0; u < U; ++u)
         if (a[u] >= 0) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) acc[k] = fmaf(g[u], x[u][k], acc[k]);
+          for (int k = 0; k < 8; ++k) acc[k] = fmaf(g[u], x[u][k], acc[k]);
         }
     }
-    float* out = p.dQ + (static_cast<int64_t>(q) * p.nq + i) * p.d + part * 16;
-#pragma unroll
-    for (int k = 0; k < 16; k += 4) *reinterpret_cast<float4*>(out + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
+    float* out = (p.splits > 1 ? p.partial + static_cast<int64_t>(blockIdx.y) * p.nQ * p.nq * p.d : p.dQ) +
+                 (static_cast<int64_t>(q) * p.nq + i) * p.d + part * 8;
+    *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(out + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
   if (bad) atomicOr(p.status, kDevErrBadInput);
+}
+
+// dQ = sum of the per-range partials, in range order (deterministic).
+__global__ void dq_reduce_kernel(const BwdParams p) {
+  const int64_t n4 = static_cast<int64_t>(p.nQ) * p.nq * p.d / 4;
+  const float4* src = reinterpret_cast<const float4*>(p.partial);
+  float4* dst = reinterpret_cast<float4*>(p.dQ);
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < n4;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = src[e];
+    for (int s = 1; s < p.splits; ++s) {
+      const float4 v = src[s * n4 + e];
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    dst[e] = a;
+  }
 }
 
 template <typename T>
@@ -292,18 +320,35 @@ maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
   // dQ
-  const int tpr = p.d / 16;
+  const int tpr = p.d / 8;
   const int rows = kBwdThreads / tpr;
   const int blocks = p.nQ * ((p.nq + rows - 1) / rows);
-  dq_kernel<T><<<blocks, kBwdThreads, 0, stream>>>(p, rows);
-  return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+  dq_kernel<T><<<dim3(blocks, p.splits), kBwdThreads, 0, stream>>>(p, rows);
+  if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+  if (p.splits > 1) {
+    const int64_t n4 = static_cast<int64_t>(p.nQ) * p.nq * p.d / 4;
+    const int64_t want = (n4 + 255) / 256;
+    dq_reduce_kernel<<<static_cast<int>(want < 4096 ? want : 4096), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+  }
+  return MAXSIM_OK;
 }
 
 }  // namespace
 
+int backward_splits(int64_t B) {
+  const int64_t s = B / 1024;  // at least ~1K documents per range
+  return static_cast<int>(s < 1 ? 1 : (s > 8 ? 8 : s));
+}
+
+size_t backward_workspace_bytes(int n_queries, int nq, int d, int64_t B) {
+  const int s = backward_splits(B);
+  return s > 1 ? static_cast<size_t>(s) * n_queries * nq * d * sizeof(float) : 0;
+}
+
 maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
                               const int32_t* doc_len, int is_bf16, const int32_t* argmax, const float* dS, float* dQ,
-                              float* dD, cudaStream_t stream) {
+                              float* dD, float* workspace, cudaStream_t stream) {
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
   BwdParams p;
@@ -319,6 +364,9 @@ maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const
   p.nq = nq;
   p.d = d;
   p.nd = nd;
+  p.nq_shift = (nq & (nq - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(nq)) : -1;
+  p.splits = backward_splits(B);
+  p.partial = workspace;
   p.status = dev->status;
   return is_bf16 ? launch_typed<__nv_bfloat16>(p, dev, stream) : launch_typed<__half>(p, dev, stream);
 }

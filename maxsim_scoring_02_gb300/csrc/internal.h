@@ -45,9 +45,10 @@ maxsim_status launch_i8(const int8_t* Q, const float* q_scale, int nq, int d, co
                         int32_t* maxdot, int32_t* argmax, cudaStream_t stream);
 
 // Backward through the saved argmax: dD (inverse CSR, destination-owned) and dQ.
+size_t backward_workspace_bytes(int n_queries, int nq, int d, int64_t B);
 maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
                               const int32_t* doc_len, int is_bf16, const int32_t* argmax, const float* dS, float* dQ,
-                              float* dD, cudaStream_t stream);
+                              float* dD, float* workspace, cudaStream_t stream);
 
 // Encodes a TMA tensor map through the driver entry point (no libcuda link).
 // Returns false if the driver call is unavailable or rejects the arguments.

@@ -132,13 +132,16 @@ struct DocWalk {
   }
 };
 
-template <bool ARGMAX>
+// MWT = M / 4 code words per token (0: runtime M); FULLK: K == 256, so every
+// uint8 code is a valid centroid and needs no clamp.
+template <int MWT, bool FULLK, bool ARGMAX>
 __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams p) {
   extern __shared__ float4 pq_smem4[];
   float* Ts = reinterpret_cast<float*>(pq_smem4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tk = lane >> 3, ii = lane & 7;
-  const int M = p.M, K = p.K, MW = M >> 2;
+  const int M = p.M, MW = MWT > 0 ? MWT : (M >> 2);
+  const int K = FULLK ? 256 : p.K;
   const uint32_t kmax = static_cast<uint32_t>(K - 1);
   const int64_t b0 = (p.B * blockIdx.x) / gridDim.x, b1 = (p.B * (blockIdx.x + 1)) / gridDim.x;
   const int64_t tsize = static_cast<int64_t>(M) * K * kGroup;  // floats per table group
@@ -202,16 +205,50 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
       __syncwarp();
       // score the staged piece: token t = 4*it + tk
       const uint32_t* cw_base = stage + bufi * (kPieceBytes / 4);
+      const float* Tl = Ts + ii;   // this lane's query token within the 8-token group
       for (int t = tk; t < cur.n; t += 4) {
         float s = 0.f;
-        for (int w = 0; w < MW; ++w) {
-          const uint32_t word = cw_base[t * MW + w];
+        if (MWT > 0) {
+          uint32_t cw[MWT > 0 ? MWT : 1];
+          if (MWT % 4 == 0) {
 #pragma unroll
-          for (int sb = 0; sb < 4; ++sb) {
-            const int m = 4 * w + sb;
-            const uint32_t raw = (word >> (8 * sb)) & 0xFFu;
-            badc |= raw > kmax;  // a code outside the codebook is clamped and reported
-            s += Ts[(m * K + static_cast<int>(min(raw, kmax))) * kGroup + ii];
+            for (int w = 0; w < MWT; w += 4) {
+              const uint4 v = *reinterpret_cast<const uint4*>(cw_base + t * MWT + w);
+              cw[w] = v.x;
+              cw[w + 1] = v.y;
+              cw[w + 2] = v.z;
+              cw[w + 3] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int w = 0; w < MWT; ++w) cw[w] = cw_base[t * MWT + w];
+          }
+#pragma unroll
+          for (int w = 0; w < MWT; ++w) {
+#pragma unroll
+            for (int sb = 0; sb < 4; ++sb) {
+              const int m = 4 * w + sb;
+              uint32_t c = (cw[w] >> (8 * sb)) & 0xFFu;
+              if (!FULLK) {
+                badc |= c > kmax;  // a code outside the codebook is clamped and reported
+                c = min(c, kmax);
+              }
+              s += Tl[(m * K) * kGroup + static_cast<int>(c) * kGroup];
+            }
+          }
+        } else {
+          for (int w = 0; w < MW; ++w) {
+            const uint32_t word = cw_base[t * MW + w];
+#pragma unroll
+            for (int sb = 0; sb < 4; ++sb) {
+              const int m = 4 * w + sb;
+              uint32_t c = (word >> (8 * sb)) & 0xFFu;
+              if (!FULLK) {
+                badc |= c > kmax;
+                c = min(c, kmax);
+              }
+              s += Tl[(m * K + static_cast<int>(c)) * kGroup];
+            }
           }
         }
         if (s > rm) {  // tokens ascend per lane: strict > keeps the lowest index
@@ -246,6 +283,23 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
     }
     if (__any_sync(0xffffffffu, badc) && lane == 0 && g == 0) atomicOr(p.status, kDevErrBadInput);
   }
+}
+
+template <int MWT, bool FULLK, bool ARGMAX>
+cudaError_t launch_pq_one(const PqParams& p, int grid, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(pq_score_kernel<MWT, FULLK, ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  pq_score_kernel<MWT, FULLK, ARGMAX><<<grid, kPqThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int MWT>
+cudaError_t launch_pq_kernel(const PqParams& p, bool fullk, bool argmax, int grid, size_t smem, cudaStream_t stream) {
+  if (fullk) return argmax ? launch_pq_one<MWT, true, true>(p, grid, smem, stream)
+                           : launch_pq_one<MWT, true, false>(p, grid, smem, stream);
+  return argmax ? launch_pq_one<MWT, false, true>(p, grid, smem, stream)
+                : launch_pq_one<MWT, false, false>(p, grid, smem, stream);
 }
 
 }  // namespace
@@ -286,13 +340,15 @@ maxsim_status launch_pq(const float* Q, int nq, int d, const float* C, int M, in
   p.argmax = argmax;
   p.status = dev->status;
   const int grid = static_cast<int>(B < dev->sm_count ? B : dev->sm_count);
+  const bool fullk = K == 256;
   cudaError_t e;
-  if (argmax) {
-    e = cudaFuncSetAttribute(pq_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess) pq_score_kernel<true><<<grid, kPqThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(pq_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess) pq_score_kernel<false><<<grid, kPqThreads, smem, stream>>>(p);
+  switch (M / 4) {
+    case 1: e = launch_pq_kernel<1>(p, fullk, argmax != nullptr, grid, smem, stream); break;
+    case 2: e = launch_pq_kernel<2>(p, fullk, argmax != nullptr, grid, smem, stream); break;
+    case 4: e = launch_pq_kernel<4>(p, fullk, argmax != nullptr, grid, smem, stream); break;
+    case 8: e = launch_pq_kernel<8>(p, fullk, argmax != nullptr, grid, smem, stream); break;
+    case 16: e = launch_pq_kernel<16>(p, fullk, argmax != nullptr, grid, smem, stream); break;
+    default: e = launch_pq_kernel<0>(p, fullk, argmax != nullptr, grid, smem, stream); break;
   }
   if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;

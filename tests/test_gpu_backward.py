@@ -125,3 +125,15 @@ def test_corrupt_argmax_is_reported_and_skipped():
     st, flags = m.maxsim_device_status()
     assert st == 1 and flags & m.DEVERR_BAD_INPUT
     assert (dD[1, 10:] == 0).all() and (dD[2] == 0).all()
+
+
+def test_backward_split_document_ranges():
+    """B >= 2048 splits the dQ sweep into document ranges whose partials are
+    added in range order from the workspace; the result must match the oracle."""
+    nQ, nq, B, nd, d = 2, 64, 3000, 40, 128
+    Q = workloads.normalized_tokens((nQ, nq, d), seed=601, dtype="bf16")
+    D = workloads.normalized_tokens((B, nd, d), seed=602, dtype="bf16")
+    L = workloads.uniform_lengths(B, 0, nd, seed=603)
+    dS = workloads.normal((nQ, B), seed=604)
+    assert m.maxsim_backward_workspace_size(nQ, nq, d, B, nd) > 0
+    _run(Q, D, L, dS)
