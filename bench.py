@@ -402,8 +402,8 @@ class I8:
 class ColPaliTrain:
     """Training step: forward with saved argmax, then the argmax-routed backward
     (inverse-CSR dD, destination-owned dQ). Q[16,1024,128], D[10000,1024,128] bf16."""
-    kernel = "fwd_tc"
-    kernel_files = ("fwd_tc.cu", "ptx.cuh")
+    kernel = "fwd_qm"
+    kernel_files = ("fwd_qm.cu", "ptx.cuh")
     bound = "tensor"
 
     def __init__(self, args, device, rank):

@@ -781,6 +781,10 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   if (d % 64 != 0 || d < 64 || d > 1024) return MAXSIM_ERR_UNSUPPORTED;
   // rows are int32 TMA coordinates and chunk indices are packed above 6 bits
   if (total_rows < 1 || total_rows > (static_cast<int64_t>(1) << 30)) return MAXSIM_ERR_UNSUPPORTED;
+  // long queries: query-major kernel (document tiles reused across 512 query rows)
+  if (fwd_qm_applicable(nq, d, total_rows))
+    return launch_fwd_qm(Q, n_queries, nq, d, D, total_rows, csr, doc_len, offsets, B, nd, is_bf16, out, argmax,
+                         stream);
   const int KB = d / 64;
 
   // Query chunk width NC = 32 * NG: as wide as nq needs (up to 256 columns,

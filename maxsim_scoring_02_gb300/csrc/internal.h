@@ -27,6 +27,13 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
                             int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
                             int is_bf16, float* out, int32_t* argmax, cudaStream_t stream);
 
+// Query-major forward for long queries (a few hundred to 1024 tokens); same
+// arguments and outputs as launch_fwd_tc, which calls it when applicable.
+bool fwd_qm_applicable(int nq, int d, int64_t total_rows);
+maxsim_status launch_fwd_qm(const void* Q, int n_queries, int nq, int d, const void* D, int64_t total_rows,
+                            int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
+                            int is_bf16, float* out, int32_t* argmax, cudaStream_t stream);
+
 // Forward scoring with fp32 inputs on the CUDA cores (FFMA).
 maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const float* D, int64_t total_rows,
                              int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,

@@ -143,6 +143,66 @@ def test_colpali_shaped_small():
     _run_padded(Q, D, None, P.TOL_LOWP)
 
 
+@pytest.mark.parametrize("nq,d,dtype", [(257, 128, "bf16"), (384, 64, "fp16"), (512, 128, "bf16"),
+                                        (513, 128, "fp16"), (500, 192, "bf16"), (1000, 128, "bf16"),
+                                        (1024, 64, "bf16"), (1100, 128, "bf16")])
+def test_long_queries(nq, d, dtype):
+    """Queries of 257..1100 tokens: resident sets of up to four 128-row query
+    blocks, at most two sets per query (1100 tokens takes the chunked passes);
+    lengths cross 128-token tile edges, with empty and length-1 documents."""
+    Q = workloads.normalized_tokens((2, nq, d), seed=nq + d, dtype=dtype)
+    D = workloads.normalized_tokens((30, 300, d), seed=nq + d + 1, dtype=dtype)
+    L = workloads.uniform_lengths(30, 0, 300, seed=nq + d + 2)
+    L[:6] = torch.tensor([0, 1, 128, 129, 256, 300], dtype=L.dtype)
+    out, am, _ = _run_padded(Q, D, L, P.TOL_LOWP)
+    assert (out[:, 0] == 0).all() and (am[:, 0] == -1).all() and (am[:, 1] == 0).all()
+    out_only = m.maxsim_score(Q.to(DEV), D.to(DEV), L.to(DEV))   # no-argmax variant: same sums
+    assert torch.equal(out_only.cpu(), out.cpu())
+
+
+def test_long_queries_varlen_and_small_batches():
+    """CSR documents with 700-token queries; batches smaller than the grid
+    (1 and 5 documents) and one not divisible by it."""
+    for B in (1, 5, 333):
+        L = workloads.lognormal_lengths(B, math.log(200), 0.8, 1, 700, seed=B)
+        off = workloads.csr_offsets(L)
+        Q = workloads.normalized_tokens((3, 700, 128), seed=B + 1, dtype="bf16")
+        Dp = workloads.normalized_tokens((int(off[-1]), 128), seed=B + 2, dtype="bf16")
+        out, am = m.maxsim_score_varlen(Q.to(DEV), Dp.to(DEV), off.to(DEV), want_argmax=True)
+        torch.cuda.synchronize()
+        assert m.maxsim_device_status() == (0, 0)
+        Qn, Dn, offn = _np(Q), _np(Dp), off.numpy()
+        ref, ref_am, gap = oracle.maxsim_varlen(Qn, Dn, offn, want_gap=True)
+        P.check_scores(out.cpu().numpy(), ref, P.TOL_LOWP)
+        norms = np.array([np.linalg.norm(Dn[offn[b]:offn[b + 1]], axis=1).max() for b in range(B)])
+        P.check_argmax(am.cpu().numpy(), ref_am, gap, P.eps_rows(Qn, norms, 128))
+
+
+def test_long_queries_bad_csr_offsets_reported():
+    Q = workloads.normalized_tokens((600, 128), seed=83, dtype="bf16").to(DEV)
+    Dp = workloads.normalized_tokens((300, 128), seed=84, dtype="bf16").to(DEV)
+    off = torch.tensor([0, 100, 50, 200, 10_000, 300], dtype=torch.int64, device=DEV)
+    out, am = m.maxsim_score_varlen(Q, Dp, off, want_argmax=True)
+    st, flags = m.maxsim_device_status()
+    assert st == 1 and flags & m.DEVERR_BAD_INPUT and flags & m.DEVERR_TIMEOUT == 0
+    ref, _, _ = oracle.maxsim_varlen(_np(Q)[None], _np(Dp), np.array([0, 100]))
+    assert abs(out[0, 0].item() - ref[0, 0]) <= P.TOL_LOWP
+    assert out[0, 1].item() == 0.0 and out[0, 3].item() == 0.0 and (am[0, 1] == -1).all()
+
+
+def test_colpali_training_size_sampled():
+    """ColPali training forward, Q[16,1024,128] x D[10000,1024,128] bf16, in the
+    benchmark's launch shape: 6 sampled documents against the oracle."""
+    nQ, nq, B, nd, d = 16, 1024, 10_000, 1024, 128
+    Q = workloads.normalized_tokens((nQ, nq, d), seed=3, dtype="bf16", device=DEV)
+    D = workloads.normalized_tokens((B, nd, d), seed=4, dtype="bf16", device=DEV)
+    out, am = m.maxsim_score(Q, D, want_argmax=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    idx = [0, 1, 4999, 5000, 8191, B - 1]
+    _check_sampled(out.cpu().numpy(), am.cpu().numpy(), Q, lambda b: _np(D[b]), idx, P.TOL_LOWP)
+
+
 def test_identity_scores_exactly_nq():
     """D := Q with exactly unit-norm sign-pattern tokens: score is exactly nq."""
     for nq, nnz in ((32, 16), (40, 64), (128, 4)):
