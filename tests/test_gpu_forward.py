@@ -143,13 +143,16 @@ def test_colpali_shaped_small():
     _run_padded(Q, D, None, P.TOL_LOWP)
 
 
-@pytest.mark.parametrize("nq,d,dtype", [(257, 128, "bf16"), (384, 64, "fp16"), (512, 128, "bf16"),
-                                        (513, 128, "fp16"), (500, 192, "bf16"), (1000, 128, "bf16"),
-                                        (1024, 64, "bf16"), (1100, 128, "bf16")])
+@pytest.mark.parametrize("nq,d,dtype", [(256, 128, "bf16"), (257, 128, "bf16"), (384, 64, "fp16"),
+                                        (512, 128, "bf16"), (513, 128, "fp16"), (500, 192, "bf16"),
+                                        (700, 128, "bf16"), (1000, 128, "bf16"), (1024, 64, "bf16"),
+                                        (1100, 128, "bf16")])
 def test_long_queries(nq, d, dtype):
-    """Queries of 257..1100 tokens: resident sets of up to four 128-row query
-    blocks, at most two sets per query (1100 tokens takes the chunked passes);
-    lengths cross 128-token tile edges, with empty and length-1 documents."""
+    """Queries of 256..1100 tokens on CTA pairs: 1 to 4 block pairs (odd and
+    even counts), the odd CTA's last block partly or wholly past nq; d=192 and
+    1100 tokens take the chunked passes. Lengths cross tile edges (tiles of
+    up to 256 columns split between the two CTAs), with empty and length-1
+    documents."""
     Q = workloads.normalized_tokens((2, nq, d), seed=nq + d, dtype=dtype)
     D = workloads.normalized_tokens((30, 300, d), seed=nq + d + 1, dtype=dtype)
     L = workloads.uniform_lengths(30, 0, 300, seed=nq + d + 2)
