@@ -12,8 +12,8 @@
 //    after a barrier wait.
 //  * N is chosen per document (a multiple of 32, at most 256) so that its
 //    tiles cover it evenly; 1024-token documents take four tiles of 256.
-//  * Two TMEM accumulators (block pair j uses accumulator j % 2), each 256
-//    columns in both CTAs. TMEM lane = query row, column = document token, so
+//  * Two TMEM accumulators (block pair j uses accumulator j % 2; a single
+//    block pair alternates between them), each 256 columns in both CTAs. TMEM lane = query row, column = document token, so
 //    the maximum over the document is thread-local (3-input max tree per
 //    32-column chunk); the argmax is searched only in a chunk that raises the
 //    running maximum. No similarity value leaves the SM.
@@ -166,6 +166,13 @@ __device__ __forceinline__ int qp_tile_n(int64_t L) {
   return static_cast<int>(n);
 }
 
+// Accumulator of block pair i at accumulator use number `uses`: i % 2, so
+// each accumulator has one consumer half; with a single block pair, uses
+// alternate between the two (both consumed, in order, by half 0).
+__device__ __forceinline__ int qp_acc_of(int nbp, int i, uint32_t uses) {
+  return nbp == 1 ? static_cast<int>(uses & 1u) : (i & 1);
+}
+
 // This pair's item range: set lane ps handles queries ps, ps + set_lanes, ...
 // over documents [b0, b0 + ndocs) of its partition; item k = (k / ndocs)-th
 // of those queries, document b0 + k % ndocs.
@@ -304,7 +311,7 @@ __device__ void qp_mma(const QpParams& p, const QpSmem& sm, const QpBars& br, ui
   const uint64_t ad0 = sdesc_k_sw128(smem_u32(sm.q)), bd0 = sdesc_k_sw128(smem_u32(sm.stages));
   const uint16_t both = 3;
   int s = 0;
-  uint32_t ph = 0, aphs = 0, quses = 0;  // aphs bit a: phase parity of accumulator a
+  uint32_t ph = 0, aphs = 0, quses = 0, uses = 0;  // aphs bit a: phase parity of accumulator a
   int prev_q = -1;
   bool ok = true;
   for (uint32_t gi = 0; ok; ++gi) {
@@ -342,8 +349,8 @@ __device__ void qp_mma(const QpParams& p, const QpSmem& sm, const QpBars& br, ui
         }
         if (!ok) break;
         tc_fence_after();
-        for (int i = 0; i < p.nbp; ++i) {
-          const int a = i & 1;
+        for (int i = 0; i < p.nbp; ++i, ++uses) {
+          const int a = qp_acc_of(p.nbp, i, uses);
           if (!mbar_poll_inl_a(br.accempty + 8 * a, ((aphs >> a) & 1u) ^ 1u, sm.abort_flag, p.status)) {
             ok = false;
             break;
@@ -489,10 +496,8 @@ __device__ void qp_epilogue(const QpParams& p, const QpSmem& sm, const QpBars& b
   const int quarter = warp & 3, half = warp >> 2;
   const int row_in_block = quarter * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-  const int a = half;
-  const uint32_t accempty_r = mapa_shared(br.accempty + 8 * a, 0);  // on the even CTA
-  const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(a * kQpMaxN);
-  uint32_t aph = 0, u = 0;
+  const uint32_t accempty_r = mapa_shared(br.accempty, 0);  // on the even CTA
+  uint32_t aphs = 0, uses = 0, u = 0;  // aphs bit a: phase parity of accumulator a
   for (uint32_t gi = 0;; ++gi) {
     const int buf = gi & 1;
     if (!mbar_wait_inl_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) return;
@@ -512,8 +517,10 @@ __device__ void qp_epilogue(const QpParams& p, const QpSmem& sm, const QpBars& b
 #pragma unroll 1
         for (int jj = 0; jj < kQpMaxBlocks / 2; ++jj) {
           if (2 * jj + half >= p.nbp) break;
-          if (!mbar_wait_inl_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
-          aph ^= 1u;
+          const int a = qp_acc_of(p.nbp, 2 * jj + half, uses++);
+          if (!mbar_wait_inl_a(br.accfull + 8 * a, (aphs >> a) & 1u, sm.abort_flag, p.status)) return;
+          aphs ^= 1u << a;
+          const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(a * kQpMaxN);
           __syncwarp();  // tcgen05.ld is warp-collective
           tc_fence_after();
           float rmj = jj ? rm1 : rm0;
@@ -537,7 +544,12 @@ __device__ void qp_epilogue(const QpParams& p, const QpSmem& sm, const QpBars& b
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(accempty_r);  // accumulator read: hand it back
+          if (lane == 0) {  // accumulator read: hand it back (on the even CTA)
+            if (rank == 0)
+              mbar_arrive_a(br.accempty + 8 * a);
+            else
+              mbar_arrive_remote(accempty_r + 8 * a);
+          }
           if (nch > kQpRound)
             qp_scan_round<ARGMAX>(r, kQpRound, nch - kQpRound, valid, t * e.N, rmj, raj);
           else

@@ -439,6 +439,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrive on an mbarrier given by its cluster address with the default
+// (CTA-scope) release: enough when the only thing the waiter needs is that
+// this thread's completed tcgen05 loads precede the signal.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // Pair MMA: D[tmem, both CTAs] (+)= A (128 rows from each CTA) * B^T (N/2
 // rows from each CTA), issued by one thread of the even CTA.
 __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
