@@ -19,10 +19,15 @@
 //
 // dq_kernel -- each CTA owns a block of (q, i) destination rows with fp32
 // accumulators in registers and sweeps one contiguous range of documents in
-// ascending order; the CTAs of a range sweep in the same order, so the
-// gathered D rows are re-served from L2. With several ranges each writes its
-// own partial dQ to the workspace and dq_reduce_kernel adds them in range
-// order -- still destination-owned, atomic-free and deterministic.
+// ascending order. A producer warp reads each document's argmax slice and
+// gathers the selected D rows into a shared-memory stage with one bulk copy
+// per row (cp.async.bulk, completing on the stage's mbarrier), several
+// documents ahead of the eight consumer warps, so the dependent argmax ->
+// row loads never stall the accumulation. The CTAs of a range sweep in the
+// same order, so the gathered rows are re-served from L2. With several
+// ranges each writes its own partial dQ to the workspace and
+// dq_reduce_kernel adds them in range order -- still destination-owned,
+// atomic-free and deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -37,6 +42,19 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
+
+// Two packed 16-bit values (low half first) as floats, exactly.
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+  return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
+}
 
 template <typename T>
 __device__ __forceinline__ float2 load2(const T* p);
@@ -208,73 +226,116 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
 }
 
 // ------------------------------------------------------------------- dQ
-// Thread layout: d / 8 threads per destination row, 8 dims each; blockIdx.y
-// picks one of `splits` contiguous document ranges. With one range the sum
-// goes straight to dQ, otherwise to partial[range] for dq_reduce_kernel.
+// Each thread owns 32 dimensions of one destination row, so a CTA holds
+// 256 / (d / 32) rows. Per document a thread copies its 64-byte slice of the
+// selected D row into its own shared-memory slot with 16-byte cp.async
+// (zero-fill for a skipped entry), kDqDepth documents ahead of the one it
+// accumulates; the argmax entries and dS values are fetched into registers
+// 2 * kDqDepth - 1 documents ahead, so neither dependent load stalls the
+// accumulation. No data is shared between threads, so the pipeline needs
+// no barrier. blockIdx.y picks one of `splits` contiguous document ranges;
+// with one range the sum goes straight to dQ, otherwise to partial[range]
+// for dq_reduce_kernel.
+constexpr int kDqThreads = 256;
+constexpr int kDqDepth = 6;                 // documents in flight per thread
+constexpr int kDqRing = 2 * kDqDepth;       // argmax / dS register ring
+
+__host__ __device__ constexpr int dq_rows(int d) { return kDqThreads / (d / 32); }
+// [depth][4 x 16 B][thread]: the v-th 16 bytes of all threads are contiguous
+__host__ __device__ constexpr size_t dq_smem_bytes() { return static_cast<size_t>(kDqDepth) * 4 * kDqThreads * 16; }
+
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads) dq_kernel(const BwdParams p, int rows_per_cta) {
+__global__ void __launch_bounds__(kDqThreads, 2) dq_kernel(const BwdParams p) {
+  extern __shared__ __align__(16) uint8_t dq_raw[];
   const int tid = threadIdx.x;
-  const int tpr = p.d / 8;
-  const int rloc = tid / tpr, part = tid - rloc * tpr;
-  const int blocks_per_q = (p.nq + rows_per_cta - 1) / rows_per_cta;
+  const int d = p.d, tpr = d / 32, R = dq_rows(d);
+  const int blocks_per_q = (p.nq + R - 1) / R;
   const int q = blockIdx.x / blocks_per_q;
-  const int i = (blockIdx.x - q * blocks_per_q) * rows_per_cta + rloc;
-  const bool active = rloc < rows_per_cta && i < p.nq && q < p.nQ;
+  const int rr = tid / tpr, part = tid - rr * tpr;
+  const int i = (blockIdx.x - q * blocks_per_q) * R + rr;
+  const bool active = rr < R && i < p.nq;  // d / 32 need not divide the thread count
   const int64_t bs = (p.B * blockIdx.y) / p.splits, be = (p.B * (blockIdx.y + 1)) / p.splits;
-  const T* Dp = static_cast<const T*>(p.D);
-  float acc[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  const int64_t n = be - bs;
+  const T* Dp = static_cast<const T*>(p.D) + part * 32;
+  const int32_t* arow = p.argmax + static_cast<int64_t>(q) * p.B * p.nq + i;
+  const float* grow = p.dS + static_cast<int64_t>(q) * p.B;
+  const uint32_t slot0 = smem_u32(dq_raw) + static_cast<uint32_t>(tid) * 16;
   bool bad = false;
-  if (active) {
-    const int32_t* arow = p.argmax + static_cast<int64_t>(q) * p.B * p.nq + i;
-    const float* grow = p.dS + static_cast<int64_t>(q) * p.B;
-    constexpr int U = 8;  // documents in flight per thread
-    for (int64_t b0 = bs; b0 < be; b0 += U) {
-      int a[U];
-      float g[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t b = b0 + u;
-        a[u] = -1;
-        g[u] = 0.f;
-        if (b < be) {
-          a[u] = __ldg(arow + b * p.nq);
-          g[u] = __ldg(grow + b);
-          const int L = doc_length(p, b);
-          if (a[u] >= 0 && (L < 0 || a[u] >= L)) {
-            bad = true;
-            a[u] = -1;
-          } else if (a[u] < -1) {
-            bad = true;
-            a[u] = -1;
-          }
+
+  // entry j (document bs + j): argmax a, dS g; a = -1 marks "nothing to add"
+  int ra[kDqRing];
+  float rg[kDqRing];
+  auto fetch = [&](int64_t j, int& a, float& g) {
+    a = -1;
+    g = 0.f;
+    if (active && j < n) {
+      const int64_t b = bs + j;
+      const int v = __ldg(arow + b * p.nq);
+      const int L = doc_length(p, b);  // -1: the document's length itself is invalid
+      if (v >= 0) {
+        if (v < L) {
+          a = v;
+          g = __ldg(grow + b);
+        } else {
+          bad = true;
         }
+      } else if (v < -1) {
+        bad = true;
       }
-      float x[U][8];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (a[u] >= 0) {
-          const T* row = Dp + ((b0 + u) * p.nd + a[u]) * static_cast<int64_t>(p.d) + part * 8;
-#pragma unroll
-          for (int k = 0; k < 8; k += 2) {
-            const float2 v = load2<T>(row + k);
-            x[u][k] = v.x;
-            x[u][k + 1] = v.y;
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (a[u] >= 0) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc[k] = fmaf(g[u], x[u][k], acc[k]);
-        }
     }
-    float* out = (p.splits > 1 ? p.partial + static_cast<int64_t>(blockIdx.y) * p.nQ * p.nq * p.d : p.dQ) +
-                 (static_cast<int64_t>(q) * p.nq + i) * p.d + part * 8;
-    *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4*>(out + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  };
+  auto issue = [&](int64_t j, int a, int slot) {
+    const uint32_t dst = slot0 + static_cast<uint32_t>(slot * 4 * kDqThreads * 16);
+    const T* src = a >= 0 ? Dp + ((bs + j) * p.nd + a) * static_cast<int64_t>(d) : Dp;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) cp_async16(dst + v * kDqThreads * 16, src + v * 8, a >= 0 ? 16u : 0u);
+  };
+
+#pragma unroll
+  for (int k = 0; k < kDqRing - 1; ++k) fetch(k, ra[k], rg[k]);
+#pragma unroll
+  for (int k = 0; k < kDqDepth - 1; ++k) {
+    issue(k, ra[k], k);
+    cp_async_commit();
+  }
+  float acc[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+  for (int64_t j0 = 0; j0 < n; j0 += kDqRing) {
+#pragma unroll
+    for (int k = 0; k < kDqRing; ++k) {
+      const int64_t j = j0 + k;
+      if (j >= n) break;
+      // copy entry j + depth - 1 (its argmax fetched depth iterations ago)
+      const int kn = (k + kDqDepth - 1) % kDqRing;
+      issue(j + kDqDepth - 1, ra[kn], (k + kDqDepth - 1) % kDqDepth);
+      cp_async_commit();
+      // fetch entry j + ring - 1 into the ring position entry j - 1 freed
+      const int kf = (k + kDqRing - 1) % kDqRing;
+      fetch(j + kDqRing - 1, ra[kf], rg[kf]);
+      cp_async_wait<kDqDepth - 1>();  // entry j's copies have landed
+      const float g = rg[k];
+      if (ra[k] >= 0) {
+        const uint8_t* src = dq_raw + (k % kDqDepth) * 4 * kDqThreads * 16 + tid * 16;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src + v * kDqThreads * 16);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float2 f = unpack2<T>(h == 0 ? w.x : h == 1 ? w.y : h == 2 ? w.z : w.w);
+            acc[v * 8 + 2 * h] = fmaf(g, f.x, acc[v * 8 + 2 * h]);
+            acc[v * 8 + 2 * h + 1] = fmaf(g, f.y, acc[v * 8 + 2 * h + 1]);
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  if (active) {
+    float* out = (p.splits > 1 ? p.partial + static_cast<int64_t>(blockIdx.y) * p.nQ * p.nq * d : p.dQ) +
+                 (static_cast<int64_t>(q) * p.nq + i) * d + part * 32;
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) *reinterpret_cast<float4*>(out + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
   }
   if (bad) atomicOr(p.status, kDevErrBadInput);
 }
@@ -320,11 +381,12 @@ maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
   // dQ
-  const int tpr = p.d / 8;
-  const int rows = kBwdThreads / tpr;
-  const int blocks = p.nQ * ((p.nq + rows - 1) / rows);
-  dq_kernel<T><<<dim3(blocks, p.splits), kBwdThreads, 0, stream>>>(p, rows);
-  if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+  const int R = dq_rows(p.d);
+  const int blocks = p.nQ * ((p.nq + R - 1) / R);
+  const size_t dq_smem = dq_smem_bytes();
+  e = cudaFuncSetAttribute(dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dq_smem));
+  if (e == cudaSuccess) dq_kernel<T><<<dim3(blocks, p.splits), kDqThreads, dq_smem, stream>>>(p);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
   if (p.splits > 1) {
     const int64_t n4 = static_cast<int64_t>(p.nQ) * p.nq * p.d / 4;
     const int64_t want = (n4 + 255) / 256;

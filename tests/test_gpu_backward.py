@@ -69,7 +69,7 @@ def test_golden_backward_zero_padded_to_d64(golden_dir):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("d", [64, 128, 192, 256, 512, 1024])
 def test_backward_random_padded(dtype, d):
     nQ, nq, B, nd = 3, 40, 60, 150
     Q = workloads.normalized_tokens((nQ, nq, d), seed=d, dtype=dtype)
