@@ -170,7 +170,7 @@ class Headline:
             w.zero_padding(self.D, self.L)
         self.out = torch.empty((1, self.B), dtype=torch.float32, device=device)
         if self.dtype == "fp32":
-            self.kernel, self.kernel_files = "fwd_f32", ("fwd_f32.cu",)
+            self.kernel, self.kernel_files = "fwd_f32", ("fwd_f32.cu", "ptx.cuh")
         esz = _ELEM[self.dtype]
         tok = float(self.L.sum().item()) if self.L is not None else float(self.B * self.nd)
         # algorithmic bytes per launch: every real document token once, the query, one fp32 score per doc

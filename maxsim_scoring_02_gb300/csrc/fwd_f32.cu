@@ -4,16 +4,34 @@
 // reading §1; FLASH-MAXSIM Figure 1 / Algorithm 2), for fp32 embeddings that
 // must be scored at fp32 accuracy: TF32 tensor-core inputs would round every
 // element to 10 mantissa bits, far outside an fp32 score tolerance, so the
-// products are formed with FFMA.
+// products are formed with FFMA. At 16 FLOP per document byte the op sits
+// above the FP32 ridge of the part (~12 FLOP/B), so the FFMA pipe bounds it.
 //
-// Block of 256 threads = 8 warps. For a 32-token query chunk and a 128-token
-// document tile, warp w owns query tokens 4w..4w+3 and lane l owns document
-// tokens l, l+32, l+64, l+96: a 4 x 4 register tile of fp32 dot products,
-// accumulated over 128-wide d-chunks staged in padded shared memory (row
-// pitch 132 floats, so the lane-strided float4 reads are conflict-free). The
-// maximum over tokens is a per-thread running maximum across tiles followed
-// by one warp butterfly; the sum over query tokens goes through shared
-// memory. Each grid-stride step handles one document for every query.
+// Work unit: a group of four documents (4 g .. 4 g + 3) scored against one
+// 32-token query chunk; the CTA tile is the chunk x four 128-token document
+// tiles (tile t of each document), accumulated over 32-dim slices of d.
+//
+// Roles (288 threads, one CTA per SM):
+//  * Producer (warp 8, lane 0): TMA loads into a ring of kStages stages; a
+//    stage holds the query chunk's 32-dim slice (4 KB) and the same slice of
+//    the four document tiles (4 x 16 KB), all with the 128-byte swizzle. A
+//    document with no tile t is not loaded.
+//  * Consumers (warps 0-7): warps 2u and 2u + 1 own document u of the group,
+//    64 tokens each; a thread holds an 8 x 8 register tile of dot products.
+//    Lane = 8 lm + ln: query rows lm + 4 r (r < 8), tokens 64 wn + ln + 8 m
+//    (m < 8). A 128-bit shared load costs two wavefronts when each even/odd
+//    lane pair reads one address and four otherwise; here the query loads
+//    are pair-shared and the document loads are not, 48 wavefronts per 256
+//    FFMA per warp, under the 64 cycles the FMA pipe needs for them. Every
+//    row of a thread has one swizzle phase per parity of r, so each 16-byte
+//    chunk address is one XOR of a per-stage base plus an immediate.
+//  * After the last d-slice of a tile, each thread folds its tile into running
+//    maxima (tokens ascending, so the lowest index wins ties); after the last
+//    tile a butterfly over the 8 token lanes and a hand-off through shared
+//    memory let warp 2u take the maximum over its document's two warps, write
+//    the argmax and add the chunk's sum into the query's score.
+// Every wait is a bounded mbarrier wait; a timeout sets MAXSIM_DEVERR_TIMEOUT
+// and the kernel drains its loads in flight and exits.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -25,36 +43,84 @@
 namespace msim {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kQC = 32;     // query tokens per chunk
-constexpr int kTT = 128;    // document tokens per tile
-constexpr int kKC = 128;    // d per chunk
-constexpr int kPitch = kKC + 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kGroup = 4;                        // documents per work unit
+constexpr int kQC = 32;                          // query tokens per chunk
+constexpr int kTT = 128;                         // document tokens per tile
+constexpr int kKC = 32;                          // d per stage (one 128-byte swizzle row)
+constexpr int kStages = 3;
+// Hand-off buffers for the per-document maximum: a consumer warp can finish up
+// to kStages items ahead of the warp that combines (one stage per item), so
+// kStages + 1 buffers keep every buffer's contents read before it is rewritten.
+constexpr int kRed = kStages + 1;
+constexpr uint32_t kQBytes = kQC * kKC * 4;      // 4 KB
+constexpr uint32_t kDBytes = kTT * kKC * 4;      // 16 KB per document tile
+constexpr uint32_t kStageBytes = kQBytes + kGroup * kDBytes;
 
 struct F32Params {
-  const float* Q;
-  const float* D;
   const int32_t* doc_len;
   const int64_t* offsets;
   int64_t B;
+  int64_t n_groups;
   int64_t total_rows;
   int nd, csr, n_queries, nq, d;
+  int evict_first;
   float* out;
   int32_t* argmax;
   unsigned* status;
 };
 
-__device__ __forceinline__ int64_t f32_doc_rows(const F32Params& p, int64_t b, int64_t& start, bool& bad) {
+struct F32Smem {
+  uint8_t* stage;     // kStages x (Q slice, 4 D slices), 1024-byte aligned
+  float* red_v;       // [kRed][8 warps][32 rows]
+  int* red_i;         // [kRed][8 warps][32 rows]
+  uint64_t* full;     // [kStages]
+  uint64_t* empty;    // [kStages]
+  uint64_t* redfull;  // [kRed]
+  int* abort_flag;
+};
+
+size_t f32_smem_bytes() {
+  return 1024 + static_cast<size_t>(kStages) * kStageBytes + 2u * kRed * kConsumerWarps * 32 * 4 +
+         (2u * kStages + kRed) * 8 + 16;
+}
+
+__device__ __forceinline__ F32Smem f32_carve(uint8_t* raw) {
+  F32Smem s;
+  s.stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.red_v = reinterpret_cast<float*>(s.stage + kStages * kStageBytes);
+  s.red_i = reinterpret_cast<int*>(s.red_v + kRed * kConsumerWarps * 32);
+  s.full = reinterpret_cast<uint64_t*>(s.red_i + kRed * kConsumerWarps * 32);
+  s.empty = s.full + kStages;
+  s.redfull = s.empty + kStages;
+  s.abort_flag = reinterpret_cast<int*>(s.redfull + kRed);
+  return s;
+}
+
+template <int OFF>
+__device__ __forceinline__ float4 lds128(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4+%5];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a), "n"(OFF));
+  return v;
+}
+
+// Tokens of document b and its first row; bad offsets / lengths give 0 tokens.
+__device__ __forceinline__ int f32_doc_rows(const F32Params& p, int64_t b, int64_t& start, bool& bad) {
   bad = false;
+  start = 0;
+  if (b >= p.B) return 0;
   if (p.csr) {
     const int64_t s = __ldg(p.offsets + b), e = __ldg(p.offsets + b + 1);
     if (s < 0 || e < s || e > p.total_rows || e - s > INT_MAX) {
       bad = true;
-      start = 0;
       return 0;
     }
     start = s;
-    return e - s;
+    return static_cast<int>(e - s);
   }
   start = b * static_cast<int64_t>(p.nd);
   const int64_t L = p.doc_len ? static_cast<int64_t>(__ldg(p.doc_len + b)) : static_cast<int64_t>(p.nd);
@@ -62,102 +128,215 @@ __device__ __forceinline__ int64_t f32_doc_rows(const F32Params& p, int64_t b, i
     bad = true;
     return 0;
   }
-  return L;
+  return static_cast<int>(L);
+}
+
+// Producer: walks the same (group, query, chunk, tile, d-slice) sequence as the
+// consumers and fills the ring.
+__device__ void f32_producer(const CUtensorMap* tm_d, const CUtensorMap* tm_q, const F32Params& p,
+                             const F32Smem& sm) {
+  const int n_qc = (p.nq + kQC - 1) / kQC;
+  const int KC = (p.d + kKC - 1) / kKC;
+  const uint64_t policy = l2_policy_evict_first();
+  const bool ef = p.evict_first != 0;
+  const uint32_t stage0 = smem_u32(sm.stage), full0 = smem_u32(sm.full), empty0 = smem_u32(sm.empty);
+  uint32_t slot = 0, phase = 0;
+  int64_t issued = 0;
+  bool ok = true;
+  for (int64_t g = blockIdx.x; ok && g < p.n_groups; g += gridDim.x) {
+    int64_t start[kGroup];
+    int T[kGroup], Tmax = 0;
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      bool bad;
+      const int L = f32_doc_rows(p, g * kGroup + u, start[u], bad);
+      T[u] = (L + kTT - 1) / kTT;
+      Tmax = T[u] > Tmax ? T[u] : Tmax;
+    }
+    if (Tmax == 0) continue;
+    for (int q = 0; ok && q < p.n_queries; ++q)
+      for (int qc = 0; ok && qc < n_qc; ++qc) {
+        const int qrow = q * p.nq + qc * kQC;
+        for (int t = 0; ok && t < Tmax; ++t) {
+          uint32_t tx = kQBytes;
+#pragma unroll
+          for (int u = 0; u < kGroup; ++u) tx += t < T[u] ? kDBytes : 0u;
+          for (int kc = 0; kc < KC; ++kc) {
+            if (!mbar_wait_a(empty0 + 8 * slot, phase ^ 1u, sm.abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = full0 + 8 * slot, dst = stage0 + slot * kStageBytes;
+            mbar_arrive_expect_tx_a(full, tx);
+            tma_load_2d_nohint_a(dst, tm_q, full, kc * kKC, qrow);
+#pragma unroll
+            for (int u = 0; u < kGroup; ++u) {
+              if (t >= T[u]) continue;
+              const int drow = static_cast<int>(start[u] + static_cast<int64_t>(t) * kTT);
+              const uint32_t ddst = dst + kQBytes + u * kDBytes;
+              if (ef)
+                tma_load_2d_a(ddst, tm_d, full, kc * kKC, drow, policy);
+              else
+                tma_load_2d_nohint_a(ddst, tm_d, full, kc * kKC, drow);
+            }
+            ++issued;
+            if (++slot == kStages) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+  }
+  if (!ok) {
+    // After an abort: wait (bounded) for every load still in flight into this CTA's ring.
+    for (int64_t y = issued > kStages ? issued - kStages : 0; y < issued; ++y)
+      mbar_wait_drain(sm.full + (y % kStages), static_cast<uint32_t>((y / kStages) & 1), p.status);
+  }
+}
+
+// One 32-dim slice: 8 chunks of 4 dims; per chunk 8 query and 8 document
+// 128-bit loads and 256 FFMA. Unrolled by two chunks: the fully unrolled
+// slice (~2200 instructions) runs slower from instruction fetch.
+__device__ __forceinline__ void f32_slice(float (&acc)[8][8], uint32_t qE, uint32_t qO, uint32_t dX) {
+#pragma unroll 2
+  for (int pc = 0; pc < 8; ++pc) {
+    const uint32_t x = static_cast<uint32_t>(pc << 4);
+    const uint32_t e = qE ^ x, o = qO ^ x, dd = dX ^ x;
+    float4 qv[8];
+    qv[0] = lds128<0>(e);
+    qv[1] = lds128<0>(o);
+    qv[2] = lds128<1024>(e);
+    qv[3] = lds128<1024>(o);
+    qv[4] = lds128<2048>(e);
+    qv[5] = lds128<2048>(o);
+    qv[6] = lds128<3072>(e);
+    qv[7] = lds128<3072>(o);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float4 dv[4];
+      if (half == 0) {
+        dv[0] = lds128<0>(dd);
+        dv[1] = lds128<1024>(dd);
+        dv[2] = lds128<2048>(dd);
+        dv[3] = lds128<3072>(dd);
+      } else {
+        dv[0] = lds128<4096>(dd);
+        dv[1] = lds128<5120>(dd);
+        dv[2] = lds128<6144>(dd);
+        dv[3] = lds128<7168>(dd);
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+          float s = acc[r][half * 4 + mm];
+          s = fmaf(qv[r].x, dv[mm].x, s);
+          s = fmaf(qv[r].y, dv[mm].y, s);
+          s = fmaf(qv[r].z, dv[mm].z, s);
+          s = fmaf(qv[r].w, dv[mm].w, s);
+          acc[r][half * 4 + mm] = s;
+        }
+    }
+  }
 }
 
 template <bool ARGMAX>
-__global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const F32Params p) {
-  extern __shared__ float4 smem4[];
-  float* Qs = reinterpret_cast<float*>(smem4);          // [kQC][kPitch]
-  float* Ds = Qs + kQC * kPitch;                         // [kTT][kPitch]
-  float* red = Ds + kTT * kPitch;                        // [8]
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_qchunks = (p.nq + kQC - 1) / kQC;
-  const int n_kc = (p.d + kKC - 1) / kKC;
+__device__ void f32_consumer(const F32Params& p, const F32Smem& sm, int warp, int lane) {
+  const int u = warp >> 1, wn = warp & 1, lm = lane >> 3, ln = lane & 7;
+  // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7).
+  // Query rows lm + 4 r: phase lm (r even) or lm + 4 (r odd); tokens
+  // 64 wn + ln + 8 m: phase ln.
+  const uint32_t qoffE = static_cast<uint32_t>(lm * 128) | static_cast<uint32_t>(lm << 4);
+  const uint32_t qoffO = static_cast<uint32_t>((lm + 4) * 128) | static_cast<uint32_t>((lm + 4) << 4);
+  const uint32_t doff = (kQBytes + u * kDBytes + static_cast<uint32_t>((wn * 64 + ln) * 128)) |
+                        static_cast<uint32_t>(ln << 4);
+  const int n_qc = (p.nq + kQC - 1) / kQC;
+  const int KC = (p.d + kKC - 1) / kKC;
+  const uint32_t stage0 = smem_u32(sm.stage);
+  const uint32_t full0 = smem_u32(sm.full), empty0 = smem_u32(sm.empty), redfull0 = smem_u32(sm.redfull);
+  uint32_t slot = 0, phase = 0, rslot = 0, rphase = 0;
+  float qsum = 0.f;
 
-  for (int64_t b = blockIdx.x; b < p.B; b += gridDim.x) {
-    int64_t start;
-    bool bad;
-    const int64_t L = f32_doc_rows(p, b, start, bad);
-    if (bad && tid == 0) atomicOr(p.status, kDevErrBadInput);
-    const int ntiles = static_cast<int>((L + kTT - 1) / kTT);
-    for (int q = 0; q < p.n_queries; ++q) {
-      float qsum = 0.f;
-      for (int qc = 0; qc < n_qchunks; ++qc) {
-        float rm[4];
-        int ra[4];
+  for (int64_t g = blockIdx.x; g < p.n_groups; g += gridDim.x) {
+    const int64_t b = g * kGroup + u;            // this warp's document
+    // this document's length and the group's tile count (every consumer warp
+    // walks the same ring sequence)
+    int L = 0, Tmax = 0;
+    bool bad = false;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+    for (int v = 0; v < kGroup; ++v) {
+      int64_t s2;
+      bool b2;
+      const int Lv = f32_doc_rows(p, g * kGroup + v, s2, b2);
+      Tmax = max(Tmax, (Lv + kTT - 1) / kTT);
+      if (v == u) {
+        L = Lv;
+        bad = b2;
+      }
+    }
+    if (bad && wn == 0 && lane == 0) atomicOr(p.status, kDevErrBadInput);
+    if (Tmax == 0) {
+      // every document of the group is empty (or rejected): score 0, argmax -1
+      if (wn == 0 && b < p.B) {
+        for (int q = lane; q < p.n_queries; q += 32) p.out[static_cast<int64_t>(q) * p.B + b] = 0.f;
+        if (ARGMAX)
+          for (int64_t i = lane; i < static_cast<int64_t>(p.n_queries) * p.nq; i += 32) {
+            const int64_t q = i / p.nq, qi = i - q * p.nq;
+            p.argmax[(q * p.B + b) * p.nq + qi] = -1;
+          }
+      }
+      continue;
+    }
+    for (int q = 0; q < p.n_queries; ++q) {
+      for (int qc = 0; qc < n_qc; ++qc) {
+        float rm[8];
+        int ra[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
           rm[r] = -INFINITY;
           ra[r] = INT_MAX;
         }
-        for (int t = 0; t < ntiles; ++t) {
-          float acc[4][4];
+        for (int t = 0; t < Tmax; ++t) {
+          float acc[8][8];
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
+          for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int m = 0; m < 4; ++m) acc[r][m] = 0.f;
-          for (int kc = 0; kc < n_kc; ++kc) {
-            const int k0 = kc * kKC;
-            const int kw = min(kKC, p.d - k0);   // multiple of 4
-            const int kw4 = kw >> 2;
-            __syncthreads();
-            // stage the query chunk (rows past nq read as 0)
-            for (int f = tid; f < kQC * kw4; f += kThreads) {
-              const int r = f / kw4, c4 = f % kw4;
-              const int qi = qc * kQC + r;
-              float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (qi < p.nq)
-                v = __ldg(reinterpret_cast<const float4*>(p.Q + (static_cast<int64_t>(q) * p.nq + qi) * p.d + k0) + c4);
-              *reinterpret_cast<float4*>(Qs + r * kPitch + c4 * 4) = v;
+            for (int m = 0; m < 8; ++m) acc[r][m] = 0.f;
+          // a warp whose 64 tokens of this tile all lie past L only keeps the ring moving
+          const bool active = t * kTT + wn * 64 < L;
+          for (int kc = 0; kc < KC; ++kc) {
+            if (!mbar_wait_a(full0 + 8 * slot, phase, sm.abort_flag, p.status)) return;
+            if (active) {
+              const uint32_t st = stage0 + slot * kStageBytes;
+              f32_slice(acc, st + qoffE, st + qoffO, st + doff);
             }
-            // stage the document tile (rows past L read as 0, masked below)
-            for (int f = tid; f < kTT * kw4; f += kThreads) {
-              const int r = f / kw4, c4 = f % kw4;
-              const int64_t j = static_cast<int64_t>(t) * kTT + r;
-              float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (j < L) v = __ldg(reinterpret_cast<const float4*>(p.D + (start + j) * p.d + k0) + c4);
-              *reinterpret_cast<float4*>(Ds + r * kPitch + c4 * 4) = v;
-            }
-            __syncthreads();
-            for (int k = 0; k < kw; k += 4) {
-              float4 qv[4], dv[4];
-#pragma unroll
-              for (int r = 0; r < 4; ++r) qv[r] = *reinterpret_cast<const float4*>(Qs + (warp * 4 + r) * kPitch + k);
-#pragma unroll
-              for (int m = 0; m < 4; ++m) dv[m] = *reinterpret_cast<const float4*>(Ds + (lane + 32 * m) * kPitch + k);
-#pragma unroll
-              for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  float s = acc[r][m];
-                  s = fmaf(qv[r].x, dv[m].x, s);
-                  s = fmaf(qv[r].y, dv[m].y, s);
-                  s = fmaf(qv[r].z, dv[m].z, s);
-                  s = fmaf(qv[r].w, dv[m].w, s);
-                  acc[r][m] = s;
-                }
+            mbar_arrive_a(empty0 + 8 * slot);
+            if (++slot == kStages) {
+              slot = 0;
+              phase ^= 1u;
             }
           }
-          // fold the tile into the running maxima (tokens ascending per thread)
+          if (active) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int64_t j = static_cast<int64_t>(t) * kTT + lane + 32 * m;
-            if (j < L) {
+            for (int m = 0; m < 8; ++m) {
+              const int j = t * kTT + wn * 64 + ln + 8 * m;
+              if (j < L) {
 #pragma unroll
-              for (int r = 0; r < 4; ++r)
-                if (acc[r][m] > rm[r]) {
-                  rm[r] = acc[r][m];
-                  ra[r] = static_cast<int>(j);
-                }
+                for (int r = 0; r < 8; ++r)
+                  if (acc[r][m] > rm[r]) {
+                    rm[r] = acc[r][m];
+                    ra[r] = j;
+                  }
+              }
             }
           }
         }
-        // warp butterfly: max over the 32 lanes, lowest index on ties
+        // maximum over the 8 token lanes, lowest index on ties
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < 8; ++r) {
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
+          for (int o = 1; o <= 4; o <<= 1) {
             const float v2 = __shfl_xor_sync(0xffffffffu, rm[r], o);
             const int i2 = __shfl_xor_sync(0xffffffffu, ra[r], o);
             if (v2 > rm[r] || (v2 == rm[r] && i2 < ra[r])) {
@@ -166,29 +345,76 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(const F32Params p) {
             }
           }
         }
-        float part = 0.f;
-        if (lane == 0) {
+        float* rv = sm.red_v + (rslot * kConsumerWarps + warp) * 32;
+        int* ri = sm.red_i + (rslot * kConsumerWarps + warp) * 32;
+        if (ln == 0) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int qi = qc * kQC + warp * 4 + r;
-            if (qi < p.nq) {
-              if (L > 0) part += rm[r];
-              if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + b) * p.nq + qi] = L > 0 ? ra[r] : -1;
-            }
+          for (int r = 0; r < 8; ++r) {
+            rv[lm + 4 * r] = rm[r];
+            ri[lm + 4 * r] = ra[r];
           }
-          red[warp] = part;
         }
-        __syncthreads();
-        if (tid == 0) {
-          float s = 0.f;
-          for (int w = 0; w < 8; ++w) s += red[w];
-          qsum += s;
+        mbar_arrive_a(redfull0 + 8 * rslot);
+        if (wn == 0) {
+          if (!mbar_wait_a(redfull0 + 8 * rslot, rphase, sm.abort_flag, p.status)) return;
+          const float* v0 = sm.red_v + (rslot * kConsumerWarps + warp) * 32;
+          const int* i0 = sm.red_i + (rslot * kConsumerWarps + warp) * 32;
+          float v = v0[lane];
+          int ix = i0[lane];
+          const float v2 = v0[32 + lane];
+          const int i2 = i0[32 + lane];
+          if (v2 > v || (v2 == v && i2 < ix)) {
+            v = v2;
+            ix = i2;
+          }
+          const int qi = qc * kQC + lane;
+          const bool valid = qi < p.nq && b < p.B;
+          if (L == 0) {
+            v = 0.f;
+            ix = -1;
+          }
+          if (ARGMAX && valid) p.argmax[(static_cast<int64_t>(q) * p.B + b) * p.nq + qi] = ix;
+          float s = valid ? v : 0.f;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          qsum = (qc == 0 ? 0.f : qsum) + s;
+          if (lane == 0 && qc == n_qc - 1 && b < p.B) p.out[static_cast<int64_t>(q) * p.B + b] = qsum;
         }
-        __syncthreads();  // red[] is rewritten by the next chunk
+        if (++rslot == kRed) {
+          rslot = 0;
+          rphase ^= 1u;
+        }
       }
-      if (tid == 0) p.out[static_cast<int64_t>(q) * p.B + b] = qsum;
     }
   }
+}
+
+template <bool ARGMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_f32_kernel(const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_q,
+                   const F32Params p) {
+  extern __shared__ uint8_t raw[];
+  const F32Smem sm = f32_carve(raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(sm.full + s, 1);
+      mbar_init(sm.empty + s, kConsumers);
+    }
+    for (int s = 0; s < kRed; ++s) mbar_init(sm.redfull + s, kConsumers);
+    *sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&tm_d);
+    tma_prefetch_desc(&tm_q);
+  }
+  __syncthreads();
+  if (warp == kConsumerWarps) {
+    if (lane == 0) f32_producer(&tm_d, &tm_q, p, sm);
+    return;
+  }
+  f32_consumer<ARGMAX>(p, sm, warp, lane);
 }
 
 }  // namespace
@@ -199,31 +425,50 @@ maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
   if (d % 4 != 0 || d > 1024) return MAXSIM_ERR_UNSUPPORTED;
+  // TMA row coordinates are 32-bit: the same row limit as the tensor-core path
+  if (total_rows > (static_cast<int64_t>(1) << 30)) return MAXSIM_ERR_UNSUPPORTED;
   F32Params p;
-  p.Q = Q;
-  p.D = D;
   p.doc_len = doc_len;
   p.offsets = offsets;
   p.B = B;
+  p.n_groups = (B + kGroup - 1) / kGroup;
   p.total_rows = total_rows;
   p.nd = nd;
   p.csr = csr;
   p.n_queries = n_queries;
   p.nq = nq;
   p.d = d;
+  // one query chunk: each document tile is read once, so stream it past L2
+  p.evict_first = (n_queries * ((nq + kQC - 1) / kQC) == 1) ? 1 : 0;
   p.out = out;
   p.argmax = argmax;
   p.status = dev->status;
-  const size_t smem = (static_cast<size_t>(kQC + kTT) * kPitch + 8) * sizeof(float);
-  const int64_t want = static_cast<int64_t>(dev->sm_count) * 2;
-  const int grid = static_cast<int>(B < want ? B : want);
+
+  // documents as a [rows, d] matrix and queries as [n_queries * nq, d], both
+  // in 32-dim x (128 | 32)-row boxes with the 128-byte swizzle; rows and
+  // dims past the ends read as zero
+  alignas(64) CUtensorMap tm_d, tm_q;
+  const uint64_t map_rows = total_rows > 0 ? static_cast<uint64_t>(total_rows) : 1;
+  const uint64_t ddims[2] = {static_cast<uint64_t>(d), map_rows};
+  const uint64_t qdims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n_queries) * nq};
+  const uint64_t strides[1] = {static_cast<uint64_t>(d) * 4};
+  const uint32_t dbox[2] = {kKC, kTT}, qbox[2] = {kKC, kQC};
+  if (!encode_tmap(&tm_d, 3, 2, const_cast<float*>(D), ddims, strides, dbox, 1) ||
+      !encode_tmap(&tm_q, 3, 2, const_cast<float*>(Q), qdims, strides, qbox, 1))
+    return MAXSIM_ERR_CUDA;
+
+  const size_t smem = f32_smem_bytes();
+  if (smem > static_cast<size_t>(dev->max_smem_optin)) return MAXSIM_ERR_UNSUPPORTED;
+  const int64_t want = dev->sm_count;
+  const int grid = static_cast<int>(p.n_groups < want ? p.n_groups : want);
   cudaError_t e;
   if (argmax) {
     e = cudaFuncSetAttribute(fwd_f32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess) fwd_f32_kernel<true><<<grid, kThreads, smem, stream>>>(p);
+    if (e == cudaSuccess) fwd_f32_kernel<true><<<grid, kThreads, smem, stream>>>(tm_d, tm_q, p);
   } else {
-    e = cudaFuncSetAttribute(fwd_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess) fwd_f32_kernel<false><<<grid, kThreads, smem, stream>>>(p);
+    e = cudaFuncSetAttribute(fwd_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e == cudaSuccess) fwd_f32_kernel<false><<<grid, kThreads, smem, stream>>>(tm_d, tm_q, p);
   }
   if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;

@@ -127,6 +127,38 @@ def test_fp32_odd_dims_and_lengths():
     _run_padded(Q, D, L, P.TOL_FP32)
 
 
+@pytest.mark.parametrize("n_queries,nq,d,B,nd", [
+    (1, 32, 4, 700, 40),       # d below one 32-dim slice
+    (3, 33, 32, 2000, 64),     # one ring stage per (document, query chunk): many hand-offs per CTA
+    (2, 64, 60, 300, 129),     # ragged d-slice and a 1-token second tile
+    (1, 1, 1024, 20, 300),     # 32 d-slices, single query token, B below the SM count
+    (4, 31, 128, 1000, 128),
+])
+def test_fp32_shapes(n_queries, nq, d, B, nd):
+    """The FFMA path over query chunking, d-slicing, token tiles and lengths
+    0, 1 and nd; NaN and Inf in the padding rows must never reach a score."""
+    Q = workloads.normalized_tokens((n_queries, nq, d), seed=nq + d, dtype="fp32")
+    D = workloads.normalized_tokens((B, nd, d), seed=B + nd, dtype="fp32")
+    L = workloads.uniform_lengths(B, 0, nd, seed=d)
+    L[0], L[1], L[-1] = 0, 1, nd
+    Dg = D.clone()
+    j = torch.arange(nd)[None, :, None]
+    pad = j >= L.long()[:, None, None]
+    Dg = torch.where(pad & (j % 2 == 0), torch.full_like(D, float("nan")), Dg)
+    Dg = torch.where(pad & (j % 2 == 1), torch.full_like(D, float("inf")), Dg)
+    out, am = m.maxsim_score(Q.to(DEV), Dg.to(DEV), L.to(DEV), want_argmax=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    workloads.zero_padding(D, L)
+    Qn, Dn = _np(Q), _np(D)
+    ref, ref_am, gap = oracle.maxsim(Qn, Dn, L.numpy(), want_gap=True)
+    P.check_scores(out.cpu().numpy(), ref, P.TOL_FP32)
+    eps = P.eps_rows(Qn, np.linalg.norm(Dn, axis=-1).max(axis=1), d)
+    P.check_argmax(am.cpu().numpy(), ref_am, gap, eps)
+    P.check_argmax_attains(am.cpu().numpy(), Qn, lambda b: Dn[b], ref_am, eps)
+    assert (out.cpu()[:, 0] == 0).all() and (am.cpu()[:, 0] == -1).all()
+
+
 @pytest.mark.parametrize("nq", [1, 17, 40, 64, 100, 256, 300])
 def test_query_lengths(nq):
     """Query chunking: NC in {32,64,128,256} plus multi-chunk queries."""
