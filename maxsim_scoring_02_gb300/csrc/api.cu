@@ -54,7 +54,7 @@ const DeviceInfo* device_info() {
 }
 
 bool encode_tmap(void* tmap, int dtype_code, int rank, void* gaddr, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle128) {
+                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -81,7 +81,9 @@ bool encode_tmap(void* tmap, int dtype_code, int rank, void* gaddr, const uint64
   }
   const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap), dt, static_cast<cuuint32_t>(rank), gaddr, gd, gs, bx,
                               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              swizzle == 1   ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : swizzle == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -11,20 +11,27 @@
 // 32-token query chunk; the CTA tile is the chunk x four 128-token document
 // tiles (tile t of each document), accumulated over 32-dim slices of d.
 //
-// Roles (288 threads, one CTA per SM):
-//  * Producer (warp 8, lane 0): TMA loads into a ring of kStages stages; a
-//    stage holds the query chunk's 32-dim slice (4 KB) and the same slice of
-//    the four document tiles (4 x 16 KB), all with the 128-byte swizzle. A
-//    document with no tile t is not loaded.
+// Roles (320 threads, one CTA per SM):
+//  * Producer (warp 8, lane 0): TMA loads of the 32-dim slice of the four
+//    document tiles (4 x 16 KB, 128-byte swizzle) into a ring of kStages
+//    stages; a document with no tile t is not loaded.
+//  * Query transposer (warp 9): writes the chunk's 32 x 32 query slice into
+//    the same stage k-major (one 36-float row per dim), read from global
+//    memory with coalesced loads (lane = dim).
 //  * Consumers (warps 0-7): warps 2u and 2u + 1 own document u of the group,
-//    64 tokens each; a thread holds an 8 x 8 register tile of dot products.
-//    Lane = 8 lm + ln: query rows lm + 4 r (r < 8), tokens 64 wn + ln + 8 m
-//    (m < 8). A 128-bit shared load costs two wavefronts when each even/odd
-//    lane pair reads one address and four otherwise; here the query loads
-//    are pair-shared and the document loads are not, 48 wavefronts per 256
-//    FFMA per warp, under the 64 cycles the FMA pipe needs for them. Every
-//    row of a thread has one swizzle phase per parity of r, so each 16-byte
-//    chunk address is one XOR of a per-stage base plus an immediate.
+//    64 tokens each; a thread holds an 8 x 8 register tile of dot products:
+//    query rows 4 lm + r and 16 + 4 lm + r (r < 4), tokens 64 wn + ln + 8 m
+//    (m < 8), lane = 8 lm + ln. Per 4-dim chunk it loads 8 float4 of the
+//    k-major query slice and 8 float4 of document rows, then issues 256 FFMA
+//    ordered (dim, token, row). With the query slice k-major, the changing
+//    query operand of consecutive FFMAs alternates register banks with the
+//    row, so each accumulator needs one fixed bank; with both operands
+//    token-major it would clash on half of them (measured: 84 against 104
+//    FMA/clk/SM in isolation). A 128-bit shared load costs two wavefronts
+//    when each even/odd lane pair reads one address, four otherwise: 48
+//    wavefronts per 256 FFMA per warp, under the 64 cycles of FMA pipe they
+//    need. The chunk loop is not unrolled: larger bodies lose more to
+//    instruction fetch than they save.
 //  * After the last d-slice of a tile, each thread folds its tile into running
 //    maxima (tokens ascending, so the lowest index wins ties); after the last
 //    tile a butterfly over the 8 token lanes and a hand-off through shared
@@ -45,7 +52,9 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kProducerWarp = kConsumerWarps;       // TMA of the document tiles
+constexpr int kQWarp = kConsumerWarps + 1;          // k-major copy of the query slice
+constexpr int kThreads = kConsumers + 64;
 constexpr int kGroup = 4;                        // documents per work unit
 constexpr int kQC = 32;                          // query tokens per chunk
 constexpr int kTT = 128;                         // document tokens per tile
@@ -55,9 +64,13 @@ constexpr int kStages = 3;
 // to kStages items ahead of the warp that combines (one stage per item), so
 // kStages + 1 buffers keep every buffer's contents read before it is rewritten.
 constexpr int kRed = kStages + 1;
-constexpr uint32_t kQBytes = kQC * kKC * 4;      // 4 KB
+// Query slice, k-major: kKC rows (one per k) of the chunk's 32 query tokens,
+// padded to 36 floats so the transposing writes spread over the banks.
+constexpr int kQPitch = kQC + 4;
+constexpr uint32_t kQBytes = 5120;               // kKC x kQPitch x 4 = 4608, rounded up to 1 KB
 constexpr uint32_t kDBytes = kTT * kKC * 4;      // 16 KB per document tile
 constexpr uint32_t kStageBytes = kQBytes + kGroup * kDBytes;
+static_assert(kKC * kQPitch * 4 <= kQBytes, "query slice");
 
 struct F32Params {
   const int32_t* doc_len;
@@ -132,9 +145,8 @@ __device__ __forceinline__ int f32_doc_rows(const F32Params& p, int64_t b, int64
 }
 
 // Producer: walks the same (group, query, chunk, tile, d-slice) sequence as the
-// consumers and fills the ring.
-__device__ void f32_producer(const CUtensorMap* tm_d, const CUtensorMap* tm_q, const F32Params& p,
-                             const F32Smem& sm) {
+// consumers and fills the ring with the document slices.
+__device__ void f32_producer(const CUtensorMap* tm_d, const F32Params& p, const F32Smem& sm) {
   const int n_qc = (p.nq + kQC - 1) / kQC;
   const int KC = (p.d + kKC - 1) / kKC;
   const uint64_t policy = l2_policy_evict_first();
@@ -156,9 +168,8 @@ __device__ void f32_producer(const CUtensorMap* tm_d, const CUtensorMap* tm_q, c
     if (Tmax == 0) continue;
     for (int q = 0; ok && q < p.n_queries; ++q)
       for (int qc = 0; ok && qc < n_qc; ++qc) {
-        const int qrow = q * p.nq + qc * kQC;
         for (int t = 0; ok && t < Tmax; ++t) {
-          uint32_t tx = kQBytes;
+          uint32_t tx = 0;
 #pragma unroll
           for (int u = 0; u < kGroup; ++u) tx += t < T[u] ? kDBytes : 0u;
           for (int kc = 0; kc < KC; ++kc) {
@@ -168,7 +179,6 @@ __device__ void f32_producer(const CUtensorMap* tm_d, const CUtensorMap* tm_q, c
             }
             const uint32_t full = full0 + 8 * slot, dst = stage0 + slot * kStageBytes;
             mbar_arrive_expect_tx_a(full, tx);
-            tma_load_2d_nohint_a(dst, tm_q, full, kc * kKC, qrow);
 #pragma unroll
             for (int u = 0; u < kGroup; ++u) {
               if (t >= T[u]) continue;
@@ -195,60 +205,92 @@ __device__ void f32_producer(const CUtensorMap* tm_d, const CUtensorMap* tm_q, c
   }
 }
 
-// One 32-dim slice: 8 chunks of 4 dims; per chunk 8 query and 8 document
-// 128-bit loads and 256 FFMA. Unrolled by two chunks: the fully unrolled
-// slice (~2200 instructions) runs slower from instruction fetch.
-__device__ __forceinline__ void f32_slice(float (&acc)[8][8], uint32_t qE, uint32_t qO, uint32_t dX) {
-#pragma unroll 2
-  for (int pc = 0; pc < 8; ++pc) {
-    const uint32_t x = static_cast<uint32_t>(pc << 4);
-    const uint32_t e = qE ^ x, o = qO ^ x, dd = dX ^ x;
-    float4 qv[8];
-    qv[0] = lds128<0>(e);
-    qv[1] = lds128<0>(o);
-    qv[2] = lds128<1024>(e);
-    qv[3] = lds128<1024>(o);
-    qv[4] = lds128<2048>(e);
-    qv[5] = lds128<2048>(o);
-    qv[6] = lds128<3072>(e);
-    qv[7] = lds128<3072>(o);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float4 dv[4];
-      if (half == 0) {
-        dv[0] = lds128<0>(dd);
-        dv[1] = lds128<1024>(dd);
-        dv[2] = lds128<2048>(dd);
-        dv[3] = lds128<3072>(dd);
-      } else {
-        dv[0] = lds128<4096>(dd);
-        dv[1] = lds128<5120>(dd);
-        dv[2] = lds128<6144>(dd);
-        dv[3] = lds128<7168>(dd);
-      }
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-          float s = acc[r][half * 4 + mm];
-          s = fmaf(qv[r].x, dv[mm].x, s);
-          s = fmaf(qv[r].y, dv[mm].y, s);
-          s = fmaf(qv[r].z, dv[mm].z, s);
-          s = fmaf(qv[r].w, dv[mm].w, s);
-          acc[r][half * 4 + mm] = s;
-        }
+// Query transposer (one warp): for every ring stage, the 32 x 32 query slice
+// read from global memory (lane = k) and written k-major into the stage; its
+// 32 arrivals complete the stage's full barrier together with the TMA bytes.
+__device__ void f32_qwarp(const float* __restrict__ Q, const F32Params& p, const F32Smem& sm, int lane) {
+  const int n_qc = (p.nq + kQC - 1) / kQC;
+  const int KC = (p.d + kKC - 1) / kKC;
+  const int64_t qrows = static_cast<int64_t>(p.n_queries) * p.nq;
+  const uint32_t full0 = smem_u32(sm.full), empty0 = smem_u32(sm.empty);
+  uint32_t slot = 0, phase = 0;
+  for (int64_t g = blockIdx.x; g < p.n_groups; g += gridDim.x) {
+    int Tmax = 0;
+    for (int u = 0; u < kGroup; ++u) {
+      int64_t st;
+      bool bad;
+      const int L = f32_doc_rows(p, g * kGroup + u, st, bad);
+      Tmax = max(Tmax, (L + kTT - 1) / kTT);
     }
+    if (Tmax == 0) continue;
+    for (int q = 0; q < p.n_queries; ++q)
+      for (int qc = 0; qc < n_qc; ++qc) {
+        const int64_t row0 = static_cast<int64_t>(q) * p.nq + qc * kQC;
+        for (int t = 0; t < Tmax; ++t)
+          for (int kc = 0; kc < KC; ++kc) {
+            const int k = kc * kKC + lane;
+            float v[kQC];
+#pragma unroll
+            for (int r = 0; r < kQC; ++r)
+              v[r] = (row0 + r < qrows && k < p.d) ? __ldg(Q + (row0 + r) * p.d + k) : 0.f;
+            if (!mbar_wait_a(empty0 + 8 * slot, phase ^ 1u, sm.abort_flag, p.status)) return;
+            float* dst = reinterpret_cast<float*>(sm.stage + slot * kStageBytes) + lane * kQPitch;
+#pragma unroll
+            for (int r = 0; r < kQC; r += 4) *reinterpret_cast<float4*>(dst + r) = make_float4(v[r], v[r + 1], v[r + 2], v[r + 3]);
+            mbar_arrive_a(full0 + 8 * slot);
+            if (++slot == kStages) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+      }
+  }
+}
+
+__device__ __forceinline__ float f4c(const float4& v, int c) { return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w; }
+
+// One 32-dim slice: 8 chunks of 4 dims. Per chunk: 8 query loads (k-major:
+// 4 dims x 2 groups of 4 rows) and 8 document loads (token-major, 4 dims of
+// one token each), then 256 FFMA ordered (dim, token, row): the document
+// value stays in the operand reuse cache and each accumulator's register bank
+// only has to differ from its row's, which is one fixed choice per row.
+__device__ __forceinline__ void f32_slice(float (&acc)[8][8], uint32_t qK, uint32_t dX) {
+#pragma unroll 1
+  for (int pc = 0; pc < 8; ++pc) {
+    const uint32_t qq = qK + pc * (4 * kQPitch * 4), dd = dX ^ static_cast<uint32_t>(pc << 4);
+    float4 qk[4][2], dv[8];
+    qk[0][0] = lds128<0 * kQPitch * 4>(qq);
+    qk[0][1] = lds128<0 * kQPitch * 4 + 64>(qq);
+    qk[1][0] = lds128<1 * kQPitch * 4>(qq);
+    qk[1][1] = lds128<1 * kQPitch * 4 + 64>(qq);
+    qk[2][0] = lds128<2 * kQPitch * 4>(qq);
+    qk[2][1] = lds128<2 * kQPitch * 4 + 64>(qq);
+    qk[3][0] = lds128<3 * kQPitch * 4>(qq);
+    qk[3][1] = lds128<3 * kQPitch * 4 + 64>(qq);
+    dv[0] = lds128<0>(dd);
+    dv[1] = lds128<1024>(dd);
+    dv[2] = lds128<2048>(dd);
+    dv[3] = lds128<3072>(dd);
+    dv[4] = lds128<4096>(dd);
+    dv[5] = lds128<5120>(dd);
+    dv[6] = lds128<6144>(dd);
+    dv[7] = lds128<7168>(dd);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r][m] = fmaf(f4c(qk[c][r >> 2], r & 3), f4c(dv[m], c), acc[r][m]);
   }
 }
 
 template <bool ARGMAX>
 __device__ void f32_consumer(const F32Params& p, const F32Smem& sm, int warp, int lane) {
   const int u = warp >> 1, wn = warp & 1, lm = lane >> 3, ln = lane & 7;
-  // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7).
-  // Query rows lm + 4 r: phase lm (r even) or lm + 4 (r odd); tokens
-  // 64 wn + ln + 8 m: phase ln.
-  const uint32_t qoffE = static_cast<uint32_t>(lm * 128) | static_cast<uint32_t>(lm << 4);
-  const uint32_t qoffO = static_cast<uint32_t>((lm + 4) * 128) | static_cast<uint32_t>((lm + 4) << 4);
+  // Query rows 4 lm + r and 16 + 4 lm + r (r < 4) from the k-major slice;
+  // tokens 64 wn + ln + 8 m with the 128-byte swizzle (chunk c of row j sits
+  // at chunk c ^ (j & 7), and (64 wn + ln + 8 m) & 7 = ln).
+  const uint32_t qoff = static_cast<uint32_t>(lm * 16);
   const uint32_t doff = (kQBytes + u * kDBytes + static_cast<uint32_t>((wn * 64 + ln) * 128)) |
                         static_cast<uint32_t>(ln << 4);
   const int n_qc = (p.nq + kQC - 1) / kQC;
@@ -309,7 +351,7 @@ __device__ void f32_consumer(const F32Params& p, const F32Smem& sm, int warp, in
             if (!mbar_wait_a(full0 + 8 * slot, phase, sm.abort_flag, p.status)) return;
             if (active) {
               const uint32_t st = stage0 + slot * kStageBytes;
-              f32_slice(acc, st + qoffE, st + qoffO, st + doff);
+              f32_slice(acc, st + qoff, st + doff);
             }
             mbar_arrive_a(empty0 + 8 * slot);
             if (++slot == kStages) {
@@ -350,8 +392,8 @@ __device__ void f32_consumer(const F32Params& p, const F32Smem& sm, int warp, in
         if (ln == 0) {
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            rv[lm + 4 * r] = rm[r];
-            ri[lm + 4 * r] = ra[r];
+            rv[4 * lm + (r & 3) + 16 * (r >> 2)] = rm[r];
+            ri[4 * lm + (r & 3) + 16 * (r >> 2)] = ra[r];
           }
         }
         mbar_arrive_a(redfull0 + 8 * rslot);
@@ -391,27 +433,27 @@ __device__ void f32_consumer(const F32Params& p, const F32Smem& sm, int warp, in
 
 template <bool ARGMAX>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_f32_kernel(const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_q,
-                   const F32Params p) {
+    fwd_f32_kernel(const __grid_constant__ CUtensorMap tm_d, const float* __restrict__ Q, const F32Params p) {
   extern __shared__ uint8_t raw[];
   const F32Smem sm = f32_carve(raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(sm.full + s, 1);
+      mbar_init(sm.full + s, 1 + 32);
       mbar_init(sm.empty + s, kConsumers);
     }
     for (int s = 0; s < kRed; ++s) mbar_init(sm.redfull + s, kConsumers);
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
-    tma_prefetch_desc(&tm_d);
-    tma_prefetch_desc(&tm_q);
-  }
+  if (warp == kProducerWarp && lane == 0) tma_prefetch_desc(&tm_d);
   __syncthreads();
-  if (warp == kConsumerWarps) {
-    if (lane == 0) f32_producer(&tm_d, &tm_q, p, sm);
+  if (warp == kProducerWarp) {
+    if (lane == 0) f32_producer(&tm_d, p, sm);
+    return;
+  }
+  if (warp == kQWarp) {
+    f32_qwarp(Q, p, sm, lane);
     return;
   }
   f32_consumer<ARGMAX>(p, sm, warp, lane);
@@ -444,17 +486,14 @@ maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const
   p.argmax = argmax;
   p.status = dev->status;
 
-  // documents as a [rows, d] matrix and queries as [n_queries * nq, d], both
-  // in 32-dim x (128 | 32)-row boxes with the 128-byte swizzle; rows and
-  // dims past the ends read as zero
-  alignas(64) CUtensorMap tm_d, tm_q;
+  // documents as a [rows, d] matrix in 32-dim x 128-row boxes with the
+  // 128-byte swizzle; rows and dims past the ends read as zero
+  alignas(64) CUtensorMap tm_d;
   const uint64_t map_rows = total_rows > 0 ? static_cast<uint64_t>(total_rows) : 1;
   const uint64_t ddims[2] = {static_cast<uint64_t>(d), map_rows};
-  const uint64_t qdims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n_queries) * nq};
   const uint64_t strides[1] = {static_cast<uint64_t>(d) * 4};
-  const uint32_t dbox[2] = {kKC, kTT}, qbox[2] = {kKC, kQC};
-  if (!encode_tmap(&tm_d, 3, 2, const_cast<float*>(D), ddims, strides, dbox, 1) ||
-      !encode_tmap(&tm_q, 3, 2, const_cast<float*>(Q), qdims, strides, qbox, 1))
+  const uint32_t dbox[2] = {kKC, kTT};
+  if (!encode_tmap(&tm_d, 3, 2, const_cast<float*>(D), ddims, strides, dbox, 1))
     return MAXSIM_ERR_CUDA;
 
   const size_t smem = f32_smem_bytes();
@@ -464,11 +503,11 @@ maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const
   cudaError_t e;
   if (argmax) {
     e = cudaFuncSetAttribute(fwd_f32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess) fwd_f32_kernel<true><<<grid, kThreads, smem, stream>>>(tm_d, tm_q, p);
+    if (e == cudaSuccess) fwd_f32_kernel<true><<<grid, kThreads, smem, stream>>>(tm_d, Q, p);
   } else {
     e = cudaFuncSetAttribute(fwd_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
-    if (e == cudaSuccess) fwd_f32_kernel<false><<<grid, kThreads, smem, stream>>>(tm_d, tm_q, p);
+    if (e == cudaSuccess) fwd_f32_kernel<false><<<grid, kThreads, smem, stream>>>(tm_d, Q, p);
   }
   if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;

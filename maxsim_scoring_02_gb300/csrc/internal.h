@@ -58,8 +58,10 @@ maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const
                               float* dD, float* workspace, cudaStream_t stream);
 
 // Encodes a TMA tensor map through the driver entry point (no libcuda link).
-// Returns false if the driver call is unavailable or rejects the arguments.
+// dtype_code: 0 fp16, 1 bf16, 2 uint8, 3 fp32; swizzle: 0 none, 1 128-byte,
+// 2 64-byte. Returns false if the driver call is unavailable or rejects the
+// arguments.
 bool encode_tmap(void* tmap, int dtype_code, int rank, void* gaddr, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle128);
+                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle);
 
 }  // namespace msim
