@@ -354,9 +354,9 @@ class PQ:
 
 
 class I8:
-    """INT8 x INT8 scoring with per-token symmetric scales, d=128."""
-    kernel = "i8_score"
-    kernel_files = ("i8.cu",)
+    """INT8 x INT8 scoring with per-token symmetric scales, d=128 (tcgen05, int8 -> fp16 on chip)."""
+    kernel = "i8tc"
+    kernel_files = ("i8tc.cu", "ptx.cuh")
     bound = "hbm"
 
     def __init__(self, args, device, rank):

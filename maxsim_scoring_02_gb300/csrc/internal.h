@@ -51,6 +51,12 @@ maxsim_status launch_i8(const int8_t* Q, const float* q_scale, int nq, int d, co
                         const int64_t* offsets, int64_t B, int64_t total_tokens, float* out, float* maxv,
                         int32_t* maxdot, int32_t* argmax, cudaStream_t stream);
 
+// INT8 x INT8 on tcgen05 (int8 converted to fp16 on chip; exact for d <= 256).
+bool i8tc_applicable(int nq, int d);
+maxsim_status launch_i8tc(const int8_t* Q, const float* q_scale, int nq, int d, const int8_t* D,
+                          const float* d_scale, const int64_t* offsets, int64_t B, int64_t total_tokens,
+                          float* out, float* maxv, int32_t* maxdot, int32_t* argmax, cudaStream_t stream);
+
 // Backward through the saved argmax: dD (inverse CSR, destination-owned) and dQ.
 size_t backward_workspace_bytes(int n_queries, int nq, int d, int64_t B);
 maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
