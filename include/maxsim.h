@@ -202,8 +202,11 @@ maxsim_status maxsim_score_pq_noalloc(const float *Q, int nq, int d,
  *   (dot at the argmax), argmax_out [B, nq] int32 -- each of the last three
  *   may be NULL.
  *
- * Runs on the warp-level tensor-core IMMA path (mma.sync m16n8k32 s8):
- * the tcgen05 8-bit integer MMA is not available for sm_103a.
+ * sm_103a has no tcgen05 8-bit integer MMA. For nq <= 32 and d <= 192 the
+ * int8 operands are converted to fp16 on chip and multiplied on tcgen05:
+ * int8 values and products are exact in fp16 and the partial sums (|.| <=
+ * 2^22) in the fp32 accumulator, so the dots are exact. Other shapes run on
+ * the warp-level IMMA path (mma.sync m16n8k32 s8).
  *
  * Limits: 1 <= nq <= 256; d in {64, 128, 192, 256, 384, 512, 768, 1024}
  * (so |dot| < 2^24 and (float)dot is exact); Q and D 16-byte aligned.
