@@ -18,7 +18,7 @@
 // so one lane holds all of one query token's similarities and the maximum
 // over the document is a serial scan in that lane: no cross-lane reduction.
 // The MMA work on the padding rows is far below the tensor-core budget.
-// Roles (256 threads):
+// Roles (288 threads):
 //  * Producer (warp 6): one contiguous bulk copy per tile (rows x d int8: CSR
 //    rows are contiguous) into a ring of stages, no padding rows fetched, the
 //    tile's token scales beside it (4-byte cp.async per lane, arriving on the
@@ -29,8 +29,11 @@
 //    K-major, 128-byte-swizzled operand buffers. Per 4 bytes: an XOR makes
 //    them biased bytes u = x + 128, PRMT places each under the fp16 exponent
 //    of 1024 (value 1024 + u), and one packed fp16 subtract of 1152 gives x.
-//  * MMA (warp 7, lane 0): S^T = Q (M = 128) x D_tile^T (N = rows rounded up
-//    to 16) over K = d into one of four TMEM accumulators.
+//  * MMA (lane 0 of warps 7 and 8, alternate tiles): S^T = Q (M = 128) x
+//    D_tile^T (N = rows rounded up to 16) over K = d into one of four TMEM
+//    accumulators. Each issuing thread owns one operand buffer and two
+//    accumulators: a thread's barrier polls wait behind its own MMAs, and
+//    with two threads those are the tile before last, usually complete.
 //  * Epilogue (warps 0 and 4, both on TMEM lanes 0-31 = the query tokens):
 //    documents alternate between the two warps (by index parity), so all of
 //    a document's tiles meet in one warp's registers. Per tile each lane
@@ -52,9 +55,9 @@
 namespace msim {
 namespace {
 
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 288;
 constexpr int kTcProducerWarp = 6;
-constexpr int kTcMmaWarp = 7;
+constexpr int kTcMmaWarp = 7;      // and warp 8: the second MMA thread
 constexpr int kTcRows = 128;       // document rows per tile (MMA N <= 128)
 constexpr int kTcM = 128;          // MMA M: query rows, nq <= 32 real
 constexpr int kTcAcc = 4;          // TMEM accumulators of kTcRows columns
@@ -256,9 +259,13 @@ __device__ void i8tc_converter(const I8TcParams& p, const I8TcSmem& sm, int ct) 
     const int rows = m->rows, flags = m->flags;
     if (!mbar_wait_a(sm.aempty + 8 * ab, aph ^ 1u, sm.abort_flag, p.status)) return;
     if (flags & 2) {
-      // end of work: hand the marker to the MMA thread
+      // end of work: hand the marker to both MMA threads (this buffer, then the other)
       if (ct == 0) sm.arows[ab] = -1;
       mbar_arrive_a(sm.afull + 8 * ab);
+      const uint32_t ob = ab ^ 1u, oph = ab ? aph ^ 1u : aph;
+      if (!mbar_wait_a(sm.aempty + 8 * ob, oph ^ 1u, sm.abort_flag, p.status)) return;
+      if (ct == 0) sm.arows[ob] = -1;
+      mbar_arrive_a(sm.afull + 8 * ob);
       return;
     }
     const uint32_t src = sm.s8 + slot * stage_bytes_of(kD);
@@ -282,14 +289,19 @@ __device__ void i8tc_converter(const I8TcParams& p, const I8TcSmem& sm, int ct) 
   }
 }
 
-__device__ void i8tc_mma(const I8TcParams& p, const I8TcSmem& sm, uint32_t tmem) {
+// MMA thread `par` (0 or 1): tiles n = par, par + 2, ...; operand buffer par,
+// accumulators par and par + 2.
+__device__ void i8tc_mma(const I8TcParams& p, const I8TcSmem& sm, uint32_t tmem, uint32_t par) {
   const int ksteps = p.d / 16;
   const uint32_t a_bytes = static_cast<uint32_t>(kTcRows * p.d * 2);
   const volatile int* arows = sm.arows;
-  uint32_t ab = 0, aph = 0, acc = 0, cph = 0;
+  const uint32_t ab = par;
+  uint32_t aph = 0;
   int64_t done = 0;
   bool ok = true;
-  for (;;) {
+  for (uint32_t i = 0;; ++i) {
+    // this thread's i-th tile is n = 2 i + par: accumulator n & 3, its (n >> 2)-th use
+    const uint32_t n = 2 * i + par, acc = n & 3, cph = (n >> 2) & 1;
     if (!mbar_poll_a(sm.afull + 8 * ab, aph, sm.abort_flag, p.status)) {
       ok = false;
       break;
@@ -312,20 +324,11 @@ __device__ void i8tc_mma(const I8TcParams& p, const I8TcSmem& sm, uint32_t tmem)
     umma_commit_a(sm.accfull + 8 * acc);
     umma_commit_a(sm.aempty + 8 * ab);
     ++done;
-    if (++ab == 2) {
-      ab = 0;
-      aph ^= 1u;
-    }
-    if (++acc == kTcAcc) {
-      acc = 0;
-      cph ^= 1u;
-    }
+    aph ^= 1u;
   }
   if (!ok && done > 0) {
     // the tensor core must be done with TMEM and shared memory before the CTA exits
-    const int64_t y = done - 1;
-    mbar_wait_drain(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(sm.aempty + 8 * (y & 1))),
-                    static_cast<uint32_t>((y >> 1) & 1), p.status);
+    mbar_wait_drain(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(sm.aempty + 8 * ab)), aph ^ 1u, p.status);
   }
 }
 
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) i8tc_kernel(const I8TcParams p)
   } else if (warp == kTcProducerWarp) {
     i8tc_producer(p, sm, lane);
   } else if (lane == 0) {
-    i8tc_mma(p, sm, tmem);
+    i8tc_mma(p, sm, tmem, static_cast<uint32_t>(warp - kTcMmaWarp));
   }
   __syncwarp();
   tc_fence_before();
