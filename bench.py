@@ -208,22 +208,26 @@ class Headline:
         if ev is not None:
             ev[1].record()
 
-    # end-to-end: host (pinned) -> device copy of the step's inputs, the call, result back
+    # end-to-end: the documents stay in pinned host memory and are scored
+    # through maxsim_score_streamed (chunked host -> device copies overlapped
+    # with scoring); the query is copied in and the scores back every step
+    E2E_CHUNK = 16384
+
     def e2e_setup(self):
         self.hQ = self.Q.cpu().pin_memory()
         self.hD = self.D.cpu().pin_memory()
         self.hL = self.L.cpu().pin_memory() if self.L is not None else None
         self.hout = torch.empty((1, self.B), dtype=torch.float32).pin_memory()
+        nb = self.m.maxsim_score_streamed_workspace_size(1, self.nq, self.nd, self.d, self.Q.dtype, self.E2E_CHUNK)
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=self.Q.device)
         self.h2d = self.hQ.numel() * self.hQ.element_size() + self.hD.numel() * self.hD.element_size() + (
             self.hL.numel() * 4 if self.hL is not None else 0)
         self.d2h = self.B * 4
 
     def e2e_step(self):
         self.Q.copy_(self.hQ, non_blocking=True)
-        self.D.copy_(self.hD, non_blocking=True)
-        if self.hL is not None:
-            self.L.copy_(self.hL, non_blocking=True)
-        self.m.maxsim_score(self.Q, self.D, self.L, out=self.out)
+        self.m.maxsim_score_streamed(self.Q, self.hD, self.hL, chunk_docs=self.E2E_CHUNK, out=self.out,
+                                     workspace=self.ws)
         self.hout.copy_(self.out, non_blocking=True)
 
     def cpu_sample(self, n):

@@ -189,6 +189,33 @@ maxsim_status maxsim_score_pq_noalloc(const float *Q, int nq, int d,
                                       float *out, int32_t *argmax_out, void *stream);
 
 /*
+ * maxsim_score_streamed -- maxsim_score for documents that stay in host
+ * memory, e.g. a corpus larger than GPU memory (TileMaxSim deep reading §5
+ * names it as an open limitation). Same operator and outputs as
+ * maxsim_score; per-document results are identical to scoring the same
+ * documents from device memory.
+ *   Q            device [n_queries, nq, d] (as maxsim_score)
+ *   D_host       HOST [B, nd, d] in dtype; page-locked memory (cudaHostAlloc /
+ *                torch pin_memory) lets copies overlap scoring, pageable
+ *                memory works but serialises each copy
+ *   doc_len_host HOST int32 [B] or NULL (as doc_len of maxsim_score)
+ *   out, argmax_out  device, as maxsim_score
+ *   workspace    device, 16-byte aligned, >= the size returned below
+ *   chunk_docs   documents per chunk (>= 1); two chunks of device buffers
+ *                alternate: the copy of chunk k + 1 (on a library-owned
+ *                copy stream) runs while chunk k is scored on `stream`.
+ * Returns after enqueueing; D_host, doc_len_host and the workspace must
+ * stay valid and unchanged until `stream` has completed. Errors as
+ * maxsim_score; a short workspace returns MAXSIM_ERR_WORKSPACE.
+ */
+size_t maxsim_score_streamed_workspace_size(int n_queries, int nq, int nd, int d, maxsim_dtype dtype,
+                                            int64_t chunk_docs);
+maxsim_status maxsim_score_streamed(const void *Q, int n_queries, int nq, int d, const void *D_host,
+                                    int64_t B, int nd, const int32_t *doc_len_host, maxsim_dtype dtype,
+                                    float *out, int32_t *argmax_out, void *workspace,
+                                    size_t workspace_bytes, int64_t chunk_docs, void *stream);
+
+/*
  * maxsim_score_i8 -- INT8 x INT8 scoring (FLASH-MAXSIM, Abstract) with
  * per-token symmetric scales:
  *   dot(i,j) = sum_k Q[i,k] * D[j,k]        exact int32

@@ -20,6 +20,7 @@ import torch
 
 __all__ = [
     "MaxSimError", "library_path", "load_library", "maxsim_score", "maxsim_score_varlen",
+    "maxsim_score_streamed", "maxsim_score_streamed_workspace_size",
     "maxsim_score_pq", "maxsim_score_pq_workspace_size", "maxsim_score_i8", "maxsim_backward",
     "maxsim_backward_workspace_size", "maxsim_device_status", "maxsim_version",
 ]
@@ -38,7 +39,8 @@ DEVERR_BAD_INPUT = 0x2
 # Every symbol the header declares (checked by the tests).
 EXPORTS = (
     "maxsim_version", "maxsim_status_string", "maxsim_device_status", "maxsim_score",
-    "maxsim_score_varlen", "maxsim_score_pq_workspace_size", "maxsim_score_pq", "maxsim_score_pq_noalloc",
+    "maxsim_score_varlen", "maxsim_score_streamed_workspace_size", "maxsim_score_streamed",
+    "maxsim_score_pq_workspace_size", "maxsim_score_pq", "maxsim_score_pq_noalloc",
     "maxsim_score_i8",
     "maxsim_backward_workspace_size", "maxsim_backward",
 )
@@ -77,6 +79,10 @@ def load_library():
     lib.maxsim_score.argtypes = [P, I32, I32, I32, P, I64, I32, P, I32, P, P, P]
     lib.maxsim_score_varlen.restype = I32
     lib.maxsim_score_varlen.argtypes = [P, I32, I32, I32, P, P, I64, I64, I32, P, P, P]
+    lib.maxsim_score_streamed_workspace_size.restype = SZ
+    lib.maxsim_score_streamed_workspace_size.argtypes = [I32, I32, I32, I32, I32, I64]
+    lib.maxsim_score_streamed.restype = I32
+    lib.maxsim_score_streamed.argtypes = [P, I32, I32, I32, P, I64, I32, P, I32, P, P, P, SZ, I64, P]
     lib.maxsim_score_pq_workspace_size.restype = SZ
     lib.maxsim_score_pq_workspace_size.argtypes = [I32, I32, I32]
     lib.maxsim_score_pq.restype = I32
@@ -158,6 +164,50 @@ def maxsim_score(Q, D, doc_len=None, out=None, argmax_out=None, want_argmax=Fals
     st = lib.maxsim_score(_ptr(Q3), nQ, nq, d, _ptr(D), B, nd, _ptr(doc_len), _DTYPE_CODE[Q.dtype],
                           _ptr(out), _ptr(argmax_out), _stream(stream))
     _check(st, "maxsim_score")
+    return (out, argmax_out) if argmax_out is not None else out
+
+
+def maxsim_score_streamed_workspace_size(n_queries, nq, nd, d, dtype, chunk_docs):
+    """Device bytes of the workspace of maxsim_score_streamed (no GPU needed)."""
+    return load_library().maxsim_score_streamed_workspace_size(n_queries, nq, nd, d, _DTYPE_CODE[dtype], chunk_docs)
+
+
+def maxsim_score_streamed(Q, D_host, doc_len_host=None, chunk_docs=16384, out=None, argmax_out=None,
+                          want_argmax=False, workspace=None, stream=None):
+    """Padded layout with the documents in HOST memory: D_host [B,Nd,d] and
+    doc_len_host [B] int32 (or None) are CPU tensors (page-locked, e.g.
+    ``pin_memory()``, for copies that overlap scoring); Q is on the GPU.
+    Chunks of ``chunk_docs`` documents are copied and scored in turn. Returns
+    out [n_queries,B] fp32 (and argmax [n_queries,B,nq] int32 when requested).
+    The host tensors must stay alive until the stream has completed."""
+    lib = load_library()
+    _dev(Q, "Q")
+    if not isinstance(D_host, torch.Tensor) or D_host.is_cuda or not D_host.is_contiguous() or D_host.dtype != Q.dtype:
+        raise ValueError("D_host must be a contiguous CPU tensor of Q's dtype")
+    Q3 = Q if Q.dim() == 3 else Q.unsqueeze(0)
+    nQ, nq, d = Q3.shape
+    B, nd, d2 = D_host.shape
+    if d2 != d:
+        raise ValueError("Q and D_host disagree on d")
+    if doc_len_host is not None and (doc_len_host.is_cuda or doc_len_host.dtype != torch.int32
+                                     or not doc_len_host.is_contiguous()):
+        raise ValueError("doc_len_host must be a contiguous CPU int32 tensor")
+    if out is None:
+        out = torch.empty((nQ, B), dtype=torch.float32, device=Q.device)
+    _dev(out, "out", torch.float32)
+    if want_argmax and argmax_out is None:
+        argmax_out = torch.empty((nQ, B, nq), dtype=torch.int32, device=Q.device)
+    if argmax_out is not None:
+        _dev(argmax_out, "argmax_out", torch.int32)
+    nbytes = lib.maxsim_score_streamed_workspace_size(nQ, nq, nd, d, _DTYPE_CODE[Q.dtype], chunk_docs)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=Q.device)
+    _dev(workspace, "workspace", torch.uint8)
+    st = lib.maxsim_score_streamed(_ptr(Q3), nQ, nq, d, ctypes.c_void_p(D_host.data_ptr()), B, nd,
+                                   None if doc_len_host is None else ctypes.c_void_p(doc_len_host.data_ptr()),
+                                   _DTYPE_CODE[Q.dtype], _ptr(out), _ptr(argmax_out), _ptr(workspace),
+                                   workspace.numel(), chunk_docs, _stream(stream))
+    _check(st, "maxsim_score_streamed")
     return (out, argmax_out) if argmax_out is not None else out
 
 

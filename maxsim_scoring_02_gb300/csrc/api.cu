@@ -159,6 +159,27 @@ maxsim_status maxsim_score(const void* Q, int n_queries, int nq, int d, const vo
                        argmax_out, s);
 }
 
+size_t maxsim_score_streamed_workspace_size(int n_queries, int nq, int nd, int d, maxsim_dtype dtype,
+                                            int64_t chunk_docs) {
+  if (dtype != MAXSIM_BF16 && dtype != MAXSIM_FP16 && dtype != MAXSIM_FP32) return 0;
+  return streamed_workspace_bytes(n_queries, nq, nd, d, static_cast<int>(dtype), chunk_docs);
+}
+
+maxsim_status maxsim_score_streamed(const void* Q, int n_queries, int nq, int d, const void* D_host, int64_t B, int nd,
+                                    const int32_t* doc_len_host, maxsim_dtype dtype, float* out,
+                                    int32_t* argmax_out, void* workspace, size_t workspace_bytes,
+                                    int64_t chunk_docs, void* stream) {
+  // the device-side checks of maxsim_score (D_host is checked for presence only)
+  maxsim_status st = check_common(Q, n_queries, nq, d, Q, B, dtype, out, argmax_out);
+  if (st != MAXSIM_OK) return st;
+  if (nd < 1 || chunk_docs < 1 || (doc_len_host && !aligned4(doc_len_host))) return MAXSIM_ERR_INVALID_ARG;
+  if (B == 0) return MAXSIM_OK;
+  if (!D_host || B > INT64_MAX / nd) return MAXSIM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MAXSIM_ERR_WORKSPACE;
+  return launch_streamed(Q, n_queries, nq, d, D_host, B, nd, doc_len_host, static_cast<int>(dtype), out, argmax_out,
+                         workspace, workspace_bytes, chunk_docs, static_cast<cudaStream_t>(stream));
+}
+
 maxsim_status maxsim_score_varlen(const void* Q, int n_queries, int nq, int d, const void* D_packed,
                                   const int64_t* offsets, int64_t B, int64_t total_tokens, maxsim_dtype dtype,
                                   float* out, int32_t* argmax_out, void* stream) {

@@ -57,6 +57,13 @@ maxsim_status launch_i8tc(const int8_t* Q, const float* q_scale, int nq, int d, 
                           const float* d_scale, const int64_t* offsets, int64_t B, int64_t total_tokens,
                           float* out, float* maxv, int32_t* maxdot, int32_t* argmax, cudaStream_t stream);
 
+// Scoring of documents held in host memory, in chunks through two device
+// buffers (copies overlapped with scoring). dtype: 0 bf16, 1 fp16, 2 fp32.
+size_t streamed_workspace_bytes(int n_queries, int nq, int nd, int d, int dtype, int64_t chunk_docs);
+maxsim_status launch_streamed(const void* Q, int n_queries, int nq, int d, const void* D_host, int64_t B, int nd,
+                              const int32_t* doc_len_host, int dtype, float* out, int32_t* argmax, void* workspace,
+                              size_t workspace_bytes, int64_t chunk, cudaStream_t stream);
+
 // Backward through the saved argmax: dD (inverse CSR, destination-owned) and dQ.
 size_t backward_workspace_bytes(int n_queries, int nq, int d, int64_t B);
 maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,

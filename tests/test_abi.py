@@ -62,6 +62,25 @@ def test_workspace_size_queries(lib):
     assert m.maxsim_score_pq_workspace_size(0, 16, 256) == 0
 
 
+def test_streamed_workspace_size(lib):
+    """Two document buffers and two length buffers of one chunk, plus score
+    and argmax scratch when several queries need the strided scatter (each
+    part rounded up to 16 bytes)."""
+    import torch
+    r16 = lambda x: (x + 15) // 16 * 16
+    nQ, nq, nd, d, chunk = 3, 40, 100, 64, 10
+    want = 2 * (r16(chunk * nd * d * 2) + r16(chunk * 4)) + r16(nQ * chunk * 4) + r16(nQ * chunk * nq * 4)
+    assert m.maxsim_score_streamed_workspace_size(nQ, nq, nd, d, torch.float16, chunk) == want
+    one = 2 * (r16(chunk * nd * d * 4) + r16(chunk * 4))        # one query: outputs written in place
+    assert m.maxsim_score_streamed_workspace_size(1, nq, nd, d, torch.float32, chunk) == one
+    assert m.maxsim_score_streamed_workspace_size(1, nq, nd, d, torch.float32, 0) == 0
+    # a missing workspace is rejected before any CUDA call
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert lib.maxsim_score_streamed(fake, 1, 32, 128, fake, 10, 128, None, 0, fake, None, None, 0, 4, None) == 5
+    assert lib.maxsim_score_streamed(fake, 1, 32, 128, None, 10, 128, None, 0, fake, None, fake, 1 << 20, 4, None) == 1
+
+
 def test_product_path_has_no_oracle_or_cpu_fallback():
     """The package and its C sources never import or link the oracle."""
     pkg = os.path.join(ROOT, "maxsim_scoring_02_gb300")
