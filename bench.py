@@ -457,6 +457,7 @@ class ColPaliTrain:
             b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             b0.record()
         self.m.maxsim_backward(self.Q, self.D, self.am, self.dS, dQ=self.dQ, dD=self.dD)
+        self.m.allreduce_dq(self.dQ)   # sharded documents: sum the dQ partials over ranks (no-op on one rank)
         if ev is not None:
             b1.record()
             self.bwd_events.append((b0, b1))

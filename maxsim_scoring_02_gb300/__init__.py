@@ -22,7 +22,7 @@ __all__ = [
     "MaxSimError", "library_path", "load_library", "maxsim_score", "maxsim_score_varlen",
     "maxsim_score_streamed", "maxsim_score_streamed_workspace_size",
     "maxsim_score_pq", "maxsim_score_pq_workspace_size", "maxsim_score_i8", "maxsim_backward",
-    "maxsim_backward_workspace_size", "maxsim_device_status", "maxsim_version",
+    "maxsim_backward_workspace_size", "maxsim_device_status", "maxsim_version", "allreduce_dq",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -343,3 +343,20 @@ def maxsim_backward(Q, D, argmax, dS, doc_len=None, dQ=None, dD=None, workspace=
                              0 if workspace is None else workspace.numel(), _stream(stream))
     _check(st, "maxsim_backward")
     return dQ.view(Q.shape) if Q.dim() == 2 else dQ, dD
+
+
+# ------------------------------------------------------------ sharded backward
+
+def allreduce_dq(dQ, group=None):
+    """Document-sharded training: every rank runs maxsim_backward on its own
+    documents, so its dQ holds only those documents' terms of
+    dQ[q,i,:] = sum_b dS[q,b] * D[b, argmax[q,b,i], :]; the sum over ranks is
+    the full gradient. One in-place all-reduce (sum) over ``group`` (NCCL for
+    CUDA tensors, gloo on CPU); dD rows belong to one rank's documents and
+    need no exchange (FLASH-MAXSIM, Abstract: destination-owned reduction).
+    A no-op without an initialised process group or with one rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return dQ
+    dist.all_reduce(dQ, op=dist.ReduceOp.SUM, group=group)
+    return dQ

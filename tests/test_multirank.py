@@ -59,3 +59,49 @@ def test_two_rank_timing_aggregation_and_sharding():
 def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
+
+
+def _dq_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import numpy as np
+    import oracle
+    import workloads
+    import maxsim_scoring_02_gb300 as m
+    # shared query; each rank owns different documents and their dS
+    Q = workloads.normalized_tokens((2, 6, 16), seed=5, dtype="fp32").double().numpy()
+    D = workloads.normalized_tokens((3, 7, 16), seed=100 + rank, dtype="fp32").double().numpy()
+    dS = workloads.normal((2, 3), seed=200 + rank).double().numpy()
+    _, am, _ = oracle.maxsim(Q, D)
+    dQ_local, _ = oracle.backward(Q, D, am, dS)
+    dQ = torch.tensor(dQ_local)
+    m.allreduce_dq(dQ)
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, dQ.numpy()))
+
+
+def test_sharded_backward_dq_allreduce_equals_full_gradient():
+    """Two ranks with disjoint documents: the all-reduced dQ equals the
+    oracle's dQ over the union of both ranks' documents."""
+    import numpy as np
+    import oracle
+    import workloads
+    ctx = mp.get_context("spawn")
+    qu = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dq_worker, args=(r, 2, port, qu)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(qu.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    Q = workloads.normalized_tokens((2, 6, 16), seed=5, dtype="fp32").double().numpy()
+    D = np.concatenate([workloads.normalized_tokens((3, 7, 16), seed=100 + r, dtype="fp32").double().numpy()
+                        for r in range(2)])
+    dS = np.concatenate([workloads.normal((2, 3), seed=200 + r).double().numpy() for r in range(2)], axis=1)
+    _, am, _ = oracle.maxsim(Q, D)
+    dQ_full, _ = oracle.backward(Q, D, am, dS)
+    for r in range(2):
+        np.testing.assert_allclose(res[r], dQ_full, rtol=1e-12, atol=1e-12)
