@@ -447,6 +447,9 @@ class ColPaliTrain:
                        "B": self.B, "step": "forward (scores + argmax) + backward (dQ, dD)",
                        "inputs": "L2-normalised N(0,1) bf16 tokens; dS ~ N(0,1)",
                        "l2": "inputs (%.2f GB) larger than L2; no flush" % (self.B * self.nd * self.d * 2 / 1e9)}
+        if torch.device(device).type == "cuda":
+            torch.cuda.synchronize(device)
+            torch.cuda.reset_peak_memory_stats(device)   # the footprint below counts the step, not input generation
 
     def step(self, ev=None):
         if ev is not None:
@@ -470,7 +473,13 @@ class ColPaliTrain:
         ms = sum(a.elapsed_time(b) for a, b in self.bwd_events) / max(1, len(self.bwd_events))
         nbytes = (2 * 4.0 * self.nQ * self.B * self.nq + self.B * self.nd * self.d * 2 + 4.0 * self.B * self.nd * self.d
                   + 4.0 * self.nQ * self.nq * self.d + 4.0 * self.nQ * self.B)
-        return {"backward_ms": ms, "backward_hbm_bytes": nbytes, "backward_gbs": nbytes / (ms / 1e3) / 1e9}
+        # memory footprint: this step's peak device bytes (every buffer is a torch tensor handed to the
+        # library) against the similarity tensor S [nQ,B,Nq,Nd] fp32 and its gradient that a
+        # materialising implementation would hold on top of the same inputs and outputs
+        sim_bytes = 4.0 * self.nQ * self.B * self.nq * self.nd
+        return {"backward_ms": ms, "backward_hbm_bytes": nbytes, "backward_gbs": nbytes / (ms / 1e3) / 1e9,
+                "peak_device_bytes": int(torch.cuda.max_memory_allocated()),
+                "materialising_extra_bytes": {"forward": int(sim_bytes), "training": int(2 * sim_bytes)}}
 
     def e2e_setup(self):
         self.h = [t.cpu().pin_memory() for t in (self.Q, self.D, self.dS)]
