@@ -21,6 +21,20 @@
 // buffer in shared memory with cp.async, so the next piece is in flight
 // while the current one is scored; document offsets come 32 at a time.
 // Lowest token index wins ties, as in the other paths.
+//
+// At M = 16, K = 256 (every code valid) a faster map is used. Lanes are
+// (token slot ts = lane/2 of 16, query half h = lane%2 of 4 tokens), and one
+// 128-bit load of a table row serves four query tokens. A row (code c,
+// subspace m) is 32 B; with rows in [m][c] order its bank group (address / 32
+// mod 4) would be c mod 4 -- random -- and the four rows that one quarter-warp
+// (8 lanes) reads would collide about half the time. In shared memory the
+// rows are therefore placed at c*16 + 4*(m%4) + m/4, so the bank group is the
+// subspace quadrant m/4. Lane pair p = ts%4 of a quarter-warp walks the
+// quadrants in the order p, p+1, p+2, p+3 (mod 4), so at every step its four
+// pairs read four distinct bank groups: one wavefront per quarter-warp. Each
+// quadrant's four terms are summed in order m from the first, and the token's
+// similarity is (Q0 + Q1) + (Q2 + Q3) whatever the lane, so equal codes give
+// equal scores and ties still go to the lowest token index.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -154,7 +168,16 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
   for (int g = 0; g < p.n_groups; ++g) {
     __syncthreads();
     const float4* src = reinterpret_cast<const float4*>(p.T + g * tsize);
-    for (int64_t e = tid; e < tsize / 4; e += kPqThreads) pq_smem4[e] = __ldg(src + e);
+    if constexpr (MWT == 4 && FULLK) {
+      // shared row c*16 + s holds subspace m = 4 (s % 4) + s / 4 of code c
+      for (int e = tid; e < 16 * 256 * 2; e += kPqThreads) {
+        const int row = e >> 1, c = row >> 4, sl = row & 15;
+        const int m = 4 * (sl & 3) + (sl >> 2);
+        pq_smem4[e] = __ldg(src + (m * 256 + c) * 2 + (e & 1));
+      }
+    } else {
+      for (int64_t e = tid; e < tsize / 4; e += kPqThreads) pq_smem4[e] = __ldg(src + e);
+    }
     __syncthreads();
     const int qi = g * kGroup + ii;
 
@@ -187,6 +210,8 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
     if (cur.b >= 0) issue(cur, 0);
     float rm = -INFINITY;
     int ra = INT_MAX;
+    float rm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    int ra4[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
     bool badc = false;
     while (cur.b >= 0) {
       // the next piece: rest of this document, or the next document
@@ -205,78 +230,173 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
       __syncwarp();
       // score the staged piece: token t = 4*it + tk
       const uint32_t* cw_base = stage + bufi * (kPieceBytes / 4);
-      const float* Tl = Ts + ii;   // this lane's query token within the 8-token group
-      for (int t = tk; t < cur.n; t += 4) {
-        float s = 0.f;
-        if (MWT > 0) {
-          uint32_t cw[MWT > 0 ? MWT : 1];
-          if (MWT % 4 == 0) {
+      if constexpr (MWT == 4 && FULLK) {
+        // token t = 16 * it + ts; query tokens 4 h .. 4 h + 3 of the group
+        const int ts = lane >> 1, h = lane & 1, pr = ts & 3;
+        const bool odd = pr & 1;
+        int jo[4];  // float offset of quadrant (i + pr) % 4 and this lane's half of the row
 #pragma unroll
-            for (int w = 0; w < MWT; w += 4) {
-              const uint4 v = *reinterpret_cast<const uint4*>(cw_base + t * MWT + w);
-              cw[w] = v.x;
-              cw[w + 1] = v.y;
-              cw[w + 2] = v.z;
-              cw[w + 3] = v.w;
+        for (int i = 0; i < 4; ++i) jo[i] = ((i + pr) & 3) * 8 + 4 * h;
+        for (int t = ts; t < cur.n; t += 16) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(cw_base + t * 4);
+          // word i of rw: the codes of quadrant (i + pr) % 4
+          uint32_t rw0 = cw.x, rw1 = cw.y, rw2 = cw.z, rw3 = cw.w;
+          if (pr & 1) {
+            const uint32_t x = rw0;
+            rw0 = rw1;
+            rw1 = rw2;
+            rw2 = rw3;
+            rw3 = x;
+          }
+          if (pr & 2) {
+            uint32_t x = rw0;
+            rw0 = rw2;
+            rw2 = x;
+            x = rw1;
+            rw1 = rw3;
+            rw3 = x;
+          }
+          const uint32_t rw[4] = {rw0, rw1, rw2, rw3};
+          float acc[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int c = static_cast<int>((rw[i] >> (8 * r)) & 0xFFu);
+              const float4 tv = *reinterpret_cast<const float4*>(Ts + c * 128 + 32 * r + jo[i]);
+              if (r == 0) {
+                acc[i][0] = tv.x;
+                acc[i][1] = tv.y;
+                acc[i][2] = tv.z;
+                acc[i][3] = tv.w;
+              } else {
+                acc[i][0] += tv.x;
+                acc[i][1] += tv.y;
+                acc[i][2] += tv.z;
+                acc[i][3] += tv.w;
+              }
+            }
+          // acc[i] holds quadrant (i + pr) % 4; both pairings below equal (Q0 + Q1) + (Q2 + Q3)
+          float s4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            s4[e] = (acc[0][e] + (odd ? acc[3][e] : acc[1][e])) + (acc[2][e] + (odd ? acc[1][e] : acc[3][e]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (s4[e] > rm4[e]) {  // tokens ascend per lane: strict > keeps the lowest index
+              rm4[e] = s4[e];
+              ra4[e] = cur.j0 + t;
+            }
+        }
+        __syncwarp();  // the buffer is refilled two pieces later
+        if (cur.last) {
+          // max over the 16 token slots (lanes with the same query half)
+#pragma unroll
+          for (int o = 2; o <= 16; o <<= 1)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float v2 = __shfl_xor_sync(0xffffffffu, rm4[e], o);
+              const int i2 = __shfl_xor_sync(0xffffffffu, ra4[e], o);
+              if (v2 > rm4[e] || (v2 == rm4[e] && i2 < ra4[e])) {
+                rm4[e] = v2;
+                ra4[e] = i2;
+              }
+            }
+          const bool nonempty = cur.j0 + cur.n > 0;
+          float pe[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = g * kGroup + 4 * h + e;
+            pe[e] = (nonempty && q < p.nq) ? rm4[e] : 0.f;
+            if (ARGMAX && ts == 0 && q < p.nq) p.argmax[cur.b * p.nq + q] = nonempty ? ra4[e] : -1;
+          }
+          // ((q0 + q1) + (q2 + q3)) + ((q4 + q5) + (q6 + q7))
+          float part = (pe[0] + pe[1]) + (pe[2] + pe[3]);
+          part += __shfl_xor_sync(0xffffffffu, part, 1);
+          if (lane == 0) p.out[cur.b] = (g == 0 ? 0.f : p.out[cur.b]) + part;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            rm4[e] = -INFINITY;
+            ra4[e] = INT_MAX;
+          }
+          ++k;
+        }
+      } else {
+
+        const float* Tl = Ts + ii;   // this lane's query token within the 8-token group
+        for (int t = tk; t < cur.n; t += 4) {
+          float s = 0.f;
+          if (MWT > 0) {
+            uint32_t cw[MWT > 0 ? MWT : 1];
+            if (MWT % 4 == 0) {
+  #pragma unroll
+              for (int w = 0; w < MWT; w += 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(cw_base + t * MWT + w);
+                cw[w] = v.x;
+                cw[w + 1] = v.y;
+                cw[w + 2] = v.z;
+                cw[w + 3] = v.w;
+              }
+            } else {
+  #pragma unroll
+              for (int w = 0; w < MWT; ++w) cw[w] = cw_base[t * MWT + w];
+            }
+  #pragma unroll
+            for (int w = 0; w < MWT; ++w) {
+  #pragma unroll
+              for (int sb = 0; sb < 4; ++sb) {
+                const int m = 4 * w + sb;
+                uint32_t c = (cw[w] >> (8 * sb)) & 0xFFu;
+                if (!FULLK) {
+                  badc |= c > kmax;  // a code outside the codebook is clamped and reported
+                  c = min(c, kmax);
+                }
+                s += Tl[(m * K) * kGroup + static_cast<int>(c) * kGroup];
+              }
             }
           } else {
-#pragma unroll
-            for (int w = 0; w < MWT; ++w) cw[w] = cw_base[t * MWT + w];
-          }
-#pragma unroll
-          for (int w = 0; w < MWT; ++w) {
-#pragma unroll
-            for (int sb = 0; sb < 4; ++sb) {
-              const int m = 4 * w + sb;
-              uint32_t c = (cw[w] >> (8 * sb)) & 0xFFu;
-              if (!FULLK) {
-                badc |= c > kmax;  // a code outside the codebook is clamped and reported
-                c = min(c, kmax);
+            for (int w = 0; w < MW; ++w) {
+              const uint32_t word = cw_base[t * MW + w];
+  #pragma unroll
+              for (int sb = 0; sb < 4; ++sb) {
+                const int m = 4 * w + sb;
+                uint32_t c = (word >> (8 * sb)) & 0xFFu;
+                if (!FULLK) {
+                  badc |= c > kmax;
+                  c = min(c, kmax);
+                }
+                s += Tl[(m * K + static_cast<int>(c)) * kGroup];
               }
-              s += Tl[(m * K) * kGroup + static_cast<int>(c) * kGroup];
             }
           }
-        } else {
-          for (int w = 0; w < MW; ++w) {
-            const uint32_t word = cw_base[t * MW + w];
-#pragma unroll
-            for (int sb = 0; sb < 4; ++sb) {
-              const int m = 4 * w + sb;
-              uint32_t c = (word >> (8 * sb)) & 0xFFu;
-              if (!FULLK) {
-                badc |= c > kmax;
-                c = min(c, kmax);
-              }
-              s += Tl[(m * K + static_cast<int>(c)) * kGroup];
+          if (s > rm) {  // tokens ascend per lane: strict > keeps the lowest index
+            rm = s;
+            ra = cur.j0 + t;
+          }
+        }
+        __syncwarp();  // the buffer is refilled two pieces later
+        if (cur.last) {
+          // max over the 4 token slots (lanes ii, ii+8, ii+16, ii+24)
+  #pragma unroll
+          for (int o = 8; o <= 16; o <<= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, rm, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, ra, o);
+            if (v2 > rm || (v2 == rm && i2 < ra)) {
+              rm = v2;
+              ra = i2;
             }
           }
+          const bool nonempty = cur.j0 + cur.n > 0;
+          float part = (nonempty && qi < p.nq) ? rm : 0.f;
+          if (ARGMAX && tk == 0 && qi < p.nq) p.argmax[cur.b * p.nq + qi] = nonempty ? ra : -1;
+  #pragma unroll
+          for (int o = 1; o <= 4; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          if (lane == 0) p.out[cur.b] = (g == 0 ? 0.f : p.out[cur.b]) + part;
+          rm = -INFINITY;
+          ra = INT_MAX;
+          ++k;
         }
-        if (s > rm) {  // tokens ascend per lane: strict > keeps the lowest index
-          rm = s;
-          ra = cur.j0 + t;
-        }
-      }
-      __syncwarp();  // the buffer is refilled two pieces later
-      if (cur.last) {
-        // max over the 4 token slots (lanes ii, ii+8, ii+16, ii+24)
-#pragma unroll
-        for (int o = 8; o <= 16; o <<= 1) {
-          const float v2 = __shfl_xor_sync(0xffffffffu, rm, o);
-          const int i2 = __shfl_xor_sync(0xffffffffu, ra, o);
-          if (v2 > rm || (v2 == rm && i2 < ra)) {
-            rm = v2;
-            ra = i2;
-          }
-        }
-        const bool nonempty = cur.j0 + cur.n > 0;
-        float part = (nonempty && qi < p.nq) ? rm : 0.f;
-        if (ARGMAX && tk == 0 && qi < p.nq) p.argmax[cur.b * p.nq + qi] = nonempty ? ra : -1;
-#pragma unroll
-        for (int o = 1; o <= 4; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (lane == 0) p.out[cur.b] = (g == 0 ? 0.f : p.out[cur.b]) + part;
-        rm = -INFINITY;
-        ra = INT_MAX;
-        ++k;
+  
       }
       cur = nxt;
       bufi ^= 1;
