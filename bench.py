@@ -301,7 +301,7 @@ class Varlen:
 class PQ:
     """Fused PQ scoring: M=16 subspaces x 8 dims, K=256 centroids, uint8 codes."""
     kernel = "pq_score"
-    kernel_files = ("pq.cu",)
+    kernel_files = ("pq.cu", "ptx.cuh")
     bound = "alu"
 
     def __init__(self, args, device, rank):
