@@ -81,6 +81,31 @@ def test_i8_shapes(nq, d):
     _check(*_inputs(300, nq, d, seed=nq + d, lo=1, hi=100, empty=(0,)))
 
 
+@pytest.mark.parametrize("d", [64, 128, 192])
+def test_i8_tile_boundaries(d):
+    """Runs of 0-3-token documents (up to 128 documents share one 128-row
+    tile), documents of 127, 128, 129, 255, 256 and 257 tokens starting at
+    shifting row alignments, and documents whose rows and scales are all
+    equal, so every similarity ties and the argmax must be the first token."""
+    rng = np.random.default_rng(d)
+    L = []
+    for _ in range(6):
+        L += list(rng.integers(0, 4, size=150))
+        L += [127, 128, 129, 255, 256, 257, 1, 0, 2, 5]
+    L = torch.tensor(L, dtype=torch.int64)
+    off = workloads.csr_offsets(L)
+    Qf = workloads.normalized_tokens((32, d), seed=d + 1, dtype="fp32")
+    Df = workloads.normalized_tokens((int(off[-1]), d), seed=d + 2, dtype="fp32")
+    Qi, sq = workloads.quantize_int8(Qf)
+    Di, sd = workloads.quantize_int8(Df)
+    offn = off.numpy()
+    for b in np.nonzero(L.numpy() >= 2)[0][::3]:
+        s0, e0 = int(offn[b]), int(offn[b + 1])
+        Di[s0:e0] = Di[s0]
+        sd[s0:e0] = sd[s0]
+    _check(Qi, sq, Di, sd, off)
+
+
 def test_extreme_values_exact():
     """All +-127 inputs: dots reach 127^2 * d; every partial sum must stay exact."""
     d = 1024
