@@ -24,7 +24,7 @@
  *      Figure 1 / Algorithm 2: a running maximum initialised to -inf,
  *         one scalar score per (query, document) pair.
  *
- * Readings taken where the sources are silent (each listed in the design doc):
+ * Readings taken where the sources are silent:
  *  - "cosine similarity" is the plain dot product of the given vectors;
  *    inputs are L2-normalised upstream, the operator does not normalise.
  *  - a token outside the document (padding, a CSR neighbour) takes no part
