@@ -50,7 +50,7 @@ extern "C" {
 typedef enum maxsim_status {
     MAXSIM_OK = 0,
     MAXSIM_ERR_INVALID_ARG = 1,  /* NULL/misaligned pointer, negative size, bad lengths/offsets */
-    MAXSIM_ERR_UNSUPPORTED = 2,  /* valid arguments this build does not handle (e.g. d % 64 != 0 on the tensor-core path) */
+    MAXSIM_ERR_UNSUPPORTED = 2,  /* valid arguments the library does not handle (e.g. d % 64 != 0 on the tensor-core path) */
     MAXSIM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     MAXSIM_ERR_TIMEOUT = 4,      /* a device pipeline wait gave up after its time bound */
     MAXSIM_ERR_WORKSPACE = 5     /* workspace NULL or smaller than the size query returned */
