@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -250,11 +251,13 @@ class Varlen:
     kernel_files = ("fwd_tc.cu", "ptx.cuh")
     bound = "hbm"
 
+    default_B = 500_000    # documents when --B is left at its default
+
     def __init__(self, args, device, rank):
         import maxsim_scoring_02_gb300 as m
         import workloads as w
         self.m, self.dtype, self.d, self.nq = m, args.dtype, args.d, 32
-        self.B = args.B if args.B != 100_000 else 500_000
+        self.B = args.B if args.B != 100_000 else self.default_B
         seed = rank_seed(rank) + 50
         self.L, self.off = _lognormal_csr(w, self.B, seed, device)
         self.T = int(self.off[-1].item())
@@ -304,11 +307,13 @@ class PQ:
     kernel_files = ("pq.cu", "ptx.cuh")
     bound = "alu"
 
+    default_B = 500_000    # documents when --B is left at its default
+
     def __init__(self, args, device, rank):
         import maxsim_scoring_02_gb300 as m
         import workloads as w
         self.m, self.dtype, self.d, self.nq, self.M, self.K = m, "fp32", 128, 32, 16, 256
-        self.B = args.B if args.B != 100_000 else 500_000
+        self.B = args.B if args.B != 100_000 else self.default_B
         seed = rank_seed(rank) + 60
         self.L, self.off = _lognormal_csr(w, self.B, seed, device)
         self.T = int(self.off[-1].item())
@@ -363,11 +368,13 @@ class I8:
     kernel_files = ("i8tc.cu", "ptx.cuh")
     bound = "hbm"
 
+    default_B = 500_000    # documents when --B is left at its default
+
     def __init__(self, args, device, rank):
         import maxsim_scoring_02_gb300 as m
         import workloads as w
         self.m, self.dtype, self.d, self.nq = m, "int8", 128, 32
-        self.B = args.B if args.B != 100_000 else 500_000
+        self.B = args.B if args.B != 100_000 else self.default_B
         seed = rank_seed(rank) + 70
         self.L, self.off = _lognormal_csr(w, self.B, seed, device)
         self.T = int(self.off[-1].item())
@@ -424,13 +431,14 @@ class ColPaliTrain:
     kernel = "fwd_qm"
     kernel_files = ("fwd_qm.cu", "ptx.cuh")
     bound = "tensor"
+    default_B = 10_000    # documents when --B is left at its default
 
     def __init__(self, args, device, rank):
         import maxsim_scoring_02_gb300 as m
         import workloads as w
         self.m, self.dtype, self.d = m, "bf16", 128
         self.nQ, self.nq, self.nd = 16, 1024, 1024
-        self.B = args.B if args.B != 100_000 else 10_000
+        self.B = args.B if args.B != 100_000 else self.default_B
         seed = rank_seed(rank) + 80
         self.Q = w.normalized_tokens((self.nQ, self.nq, self.d), seed=seed, dtype="bf16", device=device)
         self.D = w.normalized_tokens((self.B, self.nd, self.d), seed=seed + 1, dtype="bf16", device=device)
@@ -601,7 +609,11 @@ def run_reference(args, world, rank):
     sargs = copy.copy(args)
     sargs.B = min(args.B, n)          # the sample is drawn on the host; no GPU work in this arm
     wl = WORKLOADS[args.workload](sargs, "cpu", 0)
-    wl.config = dict(wl.config, B=args.B, workload=wl.workload.replace(f"_B{sargs.B}_", f"_B{args.B}_"))
+    full_B = args.B if args.B != 100_000 else getattr(WORKLOADS[args.workload], "default_B", args.B)
+    wl.config = dict(wl.config, B=full_B, workload=re.sub(r"_B%d(?=_|$)" % wl.B, "_B%d" % full_B, wl.workload),
+                     l2="host run: no GPU cache involved; each step scores a sample of the workload")
+    if "tokens" in wl.config:
+        wl.config["sample_tokens"] = wl.config.pop("tokens")   # the sample's, not the workload's
     fn, n = wl.cpu_sample(n)
     for _ in range(max(args.warmup, 1)):
         fn()
