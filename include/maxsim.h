@@ -206,7 +206,9 @@ maxsim_status maxsim_score_pq_noalloc(const float *Q, int nq, int d,
  *                copy stream) runs while chunk k is scored on `stream`.
  * Returns after enqueueing; D_host, doc_len_host and the workspace must
  * stay valid and unchanged until `stream` has completed. Errors as
- * maxsim_score; a short workspace returns MAXSIM_ERR_WORKSPACE.
+ * maxsim_score; a short workspace returns MAXSIM_ERR_WORKSPACE. On any other
+ * error return, the copies the call had queued have finished (the call waits
+ * for them), though kernels already queued on `stream` may still run.
  */
 size_t maxsim_score_streamed_workspace_size(int n_queries, int nq, int nd, int d, maxsim_dtype dtype,
                                             int64_t chunk_docs);

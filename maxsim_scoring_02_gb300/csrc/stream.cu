@@ -113,6 +113,9 @@ maxsim_status launch_streamed(const void* Q, int n_queries, int nq, int d, const
     }
     if (cudaEventRecord(consumed[buf], stream) != cudaSuccess) st = MAXSIM_ERR_CUDA;
   }
+  // On an error the caller's stream may not wait on every copy already queued
+  // into the workspace: finish them before returning, so the caller can free it.
+  if (st != MAXSIM_OK) cudaStreamSynchronize(cs);
   // destruction is deferred by the runtime until the recorded work completes
   for (int i = 0; i < 2; ++i) {
     if (copied[i]) cudaEventDestroy(copied[i]);
