@@ -82,7 +82,8 @@ def test_config_shaped_pq():
     _check(*_case(3000, 32, 128, 16, 256, seed=101, empty=(5, 17)))
 
 
-@pytest.mark.parametrize("nq,M,K,d", [(40, 8, 100, 64), (1, 4, 256, 32), (9, 32, 64, 128), (17, 64, 16, 256)])
+@pytest.mark.parametrize("nq,M,K,d", [(40, 8, 100, 64), (1, 4, 256, 32), (9, 32, 64, 128), (17, 64, 16, 256),
+                                     (20, 16, 256, 128), (1, 16, 256, 64)])
 def test_pq_shapes(nq, M, K, d):
     _check(*_case(400, nq, d, M, K, seed=nq + M, lo=1, hi=90, empty=(0, 399)))
 
