@@ -322,14 +322,13 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
           ++k;
         }
       } else {
-
         const float* Tl = Ts + ii;   // this lane's query token within the 8-token group
         for (int t = tk; t < cur.n; t += 4) {
           float s = 0.f;
           if (MWT > 0) {
             uint32_t cw[MWT > 0 ? MWT : 1];
             if (MWT % 4 == 0) {
-  #pragma unroll
+#pragma unroll
               for (int w = 0; w < MWT; w += 4) {
                 const uint4 v = *reinterpret_cast<const uint4*>(cw_base + t * MWT + w);
                 cw[w] = v.x;
@@ -338,12 +337,12 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
                 cw[w + 3] = v.w;
               }
             } else {
-  #pragma unroll
+#pragma unroll
               for (int w = 0; w < MWT; ++w) cw[w] = cw_base[t * MWT + w];
             }
-  #pragma unroll
+#pragma unroll
             for (int w = 0; w < MWT; ++w) {
-  #pragma unroll
+#pragma unroll
               for (int sb = 0; sb < 4; ++sb) {
                 const int m = 4 * w + sb;
                 uint32_t c = (cw[w] >> (8 * sb)) & 0xFFu;
@@ -357,7 +356,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
           } else {
             for (int w = 0; w < MW; ++w) {
               const uint32_t word = cw_base[t * MW + w];
-  #pragma unroll
+#pragma unroll
               for (int sb = 0; sb < 4; ++sb) {
                 const int m = 4 * w + sb;
                 uint32_t c = (word >> (8 * sb)) & 0xFFu;
@@ -377,7 +376,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
         __syncwarp();  // the buffer is refilled two pieces later
         if (cur.last) {
           // max over the 4 token slots (lanes ii, ii+8, ii+16, ii+24)
-  #pragma unroll
+#pragma unroll
           for (int o = 8; o <= 16; o <<= 1) {
             const float v2 = __shfl_xor_sync(0xffffffffu, rm, o);
             const int i2 = __shfl_xor_sync(0xffffffffu, ra, o);
@@ -389,14 +388,13 @@ __global__ void __launch_bounds__(kPqThreads, 1) pq_score_kernel(const PqParams 
           const bool nonempty = cur.j0 + cur.n > 0;
           float part = (nonempty && qi < p.nq) ? rm : 0.f;
           if (ARGMAX && tk == 0 && qi < p.nq) p.argmax[cur.b * p.nq + qi] = nonempty ? ra : -1;
-  #pragma unroll
+#pragma unroll
           for (int o = 1; o <= 4; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
           if (lane == 0) p.out[cur.b] = (g == 0 ? 0.f : p.out[cur.b]) + part;
           rm = -INFINITY;
           ra = INT_MAX;
           ++k;
         }
-  
       }
       cur = nxt;
       bufi ^= 1;
