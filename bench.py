@@ -447,9 +447,14 @@ class ColPaliTrain:
         self.am = torch.empty((self.nQ, self.B, self.nq), dtype=torch.int32, device=device)
         self.dQ = torch.empty((self.nQ, self.nq, self.d), dtype=torch.float32, device=device)
         self.dD = torch.empty((self.B, self.nd, self.d), dtype=torch.float32, device=device)
+        self.ws = None
+        if torch.device(device).type == "cuda":
+            nb = m.maxsim_backward_workspace_size(self.nQ, self.nq, self.d, self.B, self.nd)
+            self.ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=device)
         self.flops_per_launch = 2.0 * self.nQ * self.nq * self.B * self.nd * self.d
         self.bytes_per_launch = self.B * self.nd * self.d * 2 + 4.0 * self.nQ * self.B * self.nq
-        self.units, self.launches_per_step = self.B, 3
+        # forward, dD, dQ and (B >= 2048) the ordered sum of the dQ document ranges
+        self.units, self.launches_per_step = self.B, 4 if self.B >= 2048 else 3
         self.workload = f"colpali_train_q{self.nQ}x{self.nq}_nd{self.nd}_d{self.d}_B{self.B}_bf16"
         self.config = {"workload": self.workload, "queries": self.nQ, "Lq": self.nq, "Ld": self.nd, "d": self.d,
                        "B": self.B, "step": "forward (scores + argmax) + backward (dQ, dD)",
@@ -465,29 +470,66 @@ class ColPaliTrain:
         self.m.maxsim_score(self.Q, self.D, out=self.out, argmax_out=self.am)
         if ev is not None:
             ev[1].record()
-            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            b0.record()
-        self.m.maxsim_backward(self.Q, self.D, self.am, self.dS, dQ=self.dQ, dD=self.dD)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+        # the two halves of maxsim_backward, called separately so that each
+        # kernel has its own events: dD (inverse CSR) then dQ (+ ordered range sum)
+        self.m.maxsim_backward_dd(self.Q, self.am, self.dS, self.nd, dD=self.dD)
+        if ev is not None:
+            e[1].record()
+        self.m.maxsim_backward_dq(self.D, self.am, self.dS, dQ=self.dQ, workspace=self.ws)
         self.m.allreduce_dq(self.dQ)   # sharded documents: sum the dQ partials over ranks (no-op on one rank)
         if ev is not None:
-            b1.record()
-            self.bwd_events.append((b0, b1))
+            e[2].record()
+            self.bwd_events.append(e)
 
     bwd_events = []
 
+    def backward_bytes(self):
+        """Algorithmic HBM bytes per launch of the two backward kernels, and
+        the bytes each gathers row by row from L2 (one bf16 row per argmax
+        entry: Q rows for dD, D rows for dQ)."""
+        am = 4.0 * self.nQ * self.B * self.nq
+        ds = 4.0 * self.nQ * self.B
+        dd = am + ds + 4.0 * self.B * self.nd * self.d + 2.0 * self.nQ * self.nq * self.d
+        dq = am + ds + 2.0 * self.B * self.nd * self.d + 4.0 * self.nQ * self.nq * self.d
+        gather = 2.0 * self.nQ * self.B * self.nq * self.d
+        return {"dd_kernel": (dd, gather), "dq_kernel": (dq, gather)}
+
     def extra(self):
-        """Backward (dD + dQ kernels) time and its HBM bytes: argmax read twice,
-        D rows gathered once from HBM (re-served from L2), dD written, dQ written."""
-        ms = sum(a.elapsed_time(b) for a, b in self.bwd_events) / max(1, len(self.bwd_events))
-        nbytes = (2 * 4.0 * self.nQ * self.B * self.nq + self.B * self.nd * self.d * 2 + 4.0 * self.B * self.nd * self.d
-                  + 4.0 * self.nQ * self.nq * self.d + 4.0 * self.nQ * self.B)
+        """Backward (dD + dQ kernels) times and bytes, and the step's memory
+        footprint against what a materialising implementation would add."""
+        n = max(1, len(self.bwd_events))
+        dd_ms = sum(e[0].elapsed_time(e[1]) for e in self.bwd_events) / n
+        dq_ms = sum(e[1].elapsed_time(e[2]) for e in self.bwd_events) / n
+        bb = self.backward_bytes()
         # memory footprint: this step's peak device bytes (every buffer is a torch tensor handed to the
         # library) against the similarity tensor S [nQ,B,Nq,Nd] fp32 and its gradient that a
         # materialising implementation would hold on top of the same inputs and outputs
         sim_bytes = 4.0 * self.nQ * self.B * self.nq * self.nd
-        return {"backward_ms": ms, "backward_hbm_bytes": nbytes, "backward_gbs": nbytes / (ms / 1e3) / 1e9,
+        return {"backward_ms": dd_ms + dq_ms, "dd_ms": dd_ms, "dq_ms": dq_ms,
+                "backward_hbm_bytes": bb["dd_kernel"][0] + bb["dq_kernel"][0],
+                "backward_gbs": (bb["dd_kernel"][0] + bb["dq_kernel"][0]) / ((dd_ms + dq_ms) / 1e3) / 1e9,
                 "peak_device_bytes": int(torch.cuda.max_memory_allocated()),
                 "materialising_extra_bytes": {"forward": int(sim_bytes), "training": int(2 * sim_bytes)}}
+
+    def kernel_rooflines(self, peaks):
+        """HBM roofline of each backward kernel: algorithmic bytes / its own
+        event time, against the measured copy bandwidth; the L2 row gathers
+        are reported beside it."""
+        n = max(1, len(self.bwd_events))
+        times = {"dd_kernel": sum(e[0].elapsed_time(e[1]) for e in self.bwd_events) / n,
+                 "dq_kernel": sum(e[1].elapsed_time(e[2]) for e in self.bwd_events) / n}
+        src = kernel_source_hash(("bwd.cu", "ptx.cuh"))
+        res = {}
+        for k, (nbytes, gather) in self.backward_bytes().items():
+            ms = times[k]
+            gbs = nbytes / (ms / 1e3) / 1e9
+            res[k] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(k, src, self.workload),
+                      "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes, "kernel_ms": ms,
+                      "l2_gather_bytes_per_launch": gather, "l2_gather_gbs": gather / (ms / 1e3) / 1e9}
+        return res
 
     def e2e_setup(self):
         self.h = [t.cpu().pin_memory() for t in (self.Q, self.D, self.dS)]
@@ -757,6 +799,8 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
             "gpu_launches": wl.launches_per_step * args.steps,
         }
+        if hasattr(wl, "kernel_rooflines"):
+            line["roofline_kernels"] = dict({wl.kernel: line["roofline"]}, **wl.kernel_rooflines(peaks))
         if hasattr(wl, "extra"):
             line["extra"] = wl.extra()
         print(json.dumps(line), flush=True)

@@ -36,6 +36,11 @@
  *    document (L_b = 0) scores 0.0 and has argmax -1.
  *  - The argmax of query token i in document b is the LOWEST doc-local token
  *    index j attaining the maximum similarity.
+ *  - Per-device state: on its first call on a device the library looks up
+ *    the device addresses of its own global variables (the status word, the
+ *    table of maxsim_score_pq_noalloc) and keeps them for the life of the
+ *    process. cudaDeviceReset() invalidates them: do not reset a device
+ *    between calls into this library.
  */
 #ifndef MAXSIM_H_
 #define MAXSIM_H_
@@ -176,7 +181,9 @@ maxsim_status maxsim_score_pq(const float *Q, int nq, int d,
  *   MAXSIM_ERR_WORKSPACE before anything is launched.
  *   Set-up: the first call on each device looks up the array's device
  *   address with that device current; make that first call before any
- *   stream capture. A failed lookup returns MAXSIM_ERR_CUDA.
+ *   stream capture. A failed lookup returns MAXSIM_ERR_CUDA. The address is
+ *   kept until the process exits, so the device must not be reset
+ *   (cudaDeviceReset) between calls.
  *   Sharing: every call uses the same array, and it keeps the previous
  *   call's table. Each call rewrites every entry it reads, so no clearing is
  *   needed; but calls whose kernels overlap on the GPU (for example on two
@@ -283,6 +290,30 @@ maxsim_status maxsim_backward(const void *Q, int n_queries, int nq, int d,
                               maxsim_dtype dtype, const int32_t *argmax, const float *dS,
                               float *dQ, float *dD,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * maxsim_backward_dq -- the dQ half of maxsim_backward alone, for training
+ * with a frozen document side (pre-encoded documents: no dD is wanted).
+ * Same formula, arguments, limits, workspace and errors as maxsim_backward,
+ * without Q (dQ does not depend on it) and without dD. Runs the same kernels
+ * as the dQ half of maxsim_backward, so dQ is identical to that call's.
+ */
+maxsim_status maxsim_backward_dq(int n_queries, int nq, int d,
+                                 const void *D, int64_t B, int nd, const int32_t *doc_len,
+                                 maxsim_dtype dtype, const int32_t *argmax, const float *dS,
+                                 float *dQ, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * maxsim_backward_dd -- the dD half of maxsim_backward alone (the inverse-grid
+ * CSR and the destination-owned dD rows), for training with a frozen query
+ * side. Same formula, arguments, limits and errors as maxsim_backward,
+ * without D (dD does not depend on it), dQ and the workspace (dD needs none).
+ * dD is identical to that of maxsim_backward.
+ */
+maxsim_status maxsim_backward_dd(const void *Q, int n_queries, int nq, int d,
+                                 int64_t B, int nd, const int32_t *doc_len,
+                                 maxsim_dtype dtype, const int32_t *argmax, const float *dS,
+                                 float *dD, void *stream);
 
 #ifdef __cplusplus
 }

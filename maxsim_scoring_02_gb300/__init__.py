@@ -22,7 +22,8 @@ __all__ = [
     "MaxSimError", "library_path", "load_library", "maxsim_score", "maxsim_score_varlen",
     "maxsim_score_streamed", "maxsim_score_streamed_workspace_size",
     "maxsim_score_pq", "maxsim_score_pq_workspace_size", "maxsim_score_i8", "maxsim_backward",
-    "maxsim_backward_workspace_size", "maxsim_device_status", "maxsim_version", "allreduce_dq",
+    "maxsim_backward_workspace_size", "maxsim_backward_dq", "maxsim_backward_dd", "maxsim_device_status",
+    "maxsim_version", "allreduce_dq",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,7 @@ EXPORTS = (
     "maxsim_score_varlen", "maxsim_score_streamed_workspace_size", "maxsim_score_streamed",
     "maxsim_score_pq_workspace_size", "maxsim_score_pq", "maxsim_score_pq_noalloc",
     "maxsim_score_i8",
-    "maxsim_backward_workspace_size", "maxsim_backward",
+    "maxsim_backward_workspace_size", "maxsim_backward", "maxsim_backward_dq", "maxsim_backward_dd",
 )
 
 
@@ -95,6 +96,10 @@ def load_library():
     lib.maxsim_backward_workspace_size.argtypes = [I32, I32, I32, I64, I32]
     lib.maxsim_backward.restype = I32
     lib.maxsim_backward.argtypes = [P, I32, I32, I32, P, I64, I32, P, I32, P, P, P, P, P, SZ, P]
+    lib.maxsim_backward_dq.restype = I32
+    lib.maxsim_backward_dq.argtypes = [I32, I32, I32, P, I64, I32, P, I32, P, P, P, P, SZ, P]
+    lib.maxsim_backward_dd.restype = I32
+    lib.maxsim_backward_dd.argtypes = [P, I32, I32, I32, I64, I32, P, I32, P, P, P, P]
     _lib = lib
     return lib
 
@@ -343,6 +348,55 @@ def maxsim_backward(Q, D, argmax, dS, doc_len=None, dQ=None, dD=None, workspace=
                              0 if workspace is None else workspace.numel(), _stream(stream))
     _check(st, "maxsim_backward")
     return dQ.view(Q.shape) if Q.dim() == 2 else dQ, dD
+
+
+def maxsim_backward_dq(D, argmax, dS, nq=None, doc_len=None, dQ=None, workspace=None, stream=None):
+    """dQ only (frozen document side). D [B,Nd,d]; argmax [n_queries,B,nq]
+    int32; dS [n_queries,B] fp32. Returns dQ [n_queries,nq,d] fp32."""
+    lib = load_library()
+    _dev(D, "D")
+    _dev(argmax, "argmax", torch.int32)
+    _dev(dS, "dS", torch.float32)
+    nQ, B2, nq_a = argmax.shape
+    B, nd, d = D.shape
+    if B2 != B or dS.shape != (nQ, B):
+        raise ValueError("argmax / dS shapes do not match D")
+    if doc_len is not None:
+        _dev(doc_len, "doc_len", torch.int32)
+    if dQ is None:
+        dQ = torch.empty((nQ, nq_a, d), dtype=torch.float32, device=D.device)
+    _dev(dQ, "dQ", torch.float32)
+    ws = maxsim_backward_workspace_size(nQ, nq_a, d, B, nd)
+    if workspace is None and ws > 0:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=D.device)
+    st = lib.maxsim_backward_dq(nQ, nq_a, d, _ptr(D), B, nd, _ptr(doc_len), _DTYPE_CODE[D.dtype], _ptr(argmax),
+                                _ptr(dS), _ptr(dQ), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                _stream(stream))
+    _check(st, "maxsim_backward_dq")
+    return dQ
+
+
+def maxsim_backward_dd(Q, argmax, dS, nd, doc_len=None, dD=None, stream=None):
+    """dD only (frozen query side). Q [nq,d] or [n_queries,nq,d]; argmax
+    [n_queries,B,nq] int32; dS [n_queries,B] fp32. Returns dD [B,nd,d] fp32."""
+    lib = load_library()
+    _dev(Q, "Q")
+    _dev(argmax, "argmax", torch.int32)
+    _dev(dS, "dS", torch.float32)
+    Q3 = Q if Q.dim() == 3 else Q.unsqueeze(0)
+    nQ, nq, d = Q3.shape
+    B = argmax.shape[1]
+    if argmax.shape != (nQ, B, nq) or dS.shape != (nQ, B):
+        raise ValueError("argmax / dS shapes do not match Q")
+    if doc_len is not None:
+        _dev(doc_len, "doc_len", torch.int32)
+    if dD is None:
+        dD = torch.empty((B, nd, d), dtype=torch.float32, device=Q.device)
+    _dev(dD, "dD", torch.float32)
+    st = lib.maxsim_backward_dd(_ptr(Q3), nQ, nq, d, B, nd, _ptr(doc_len), _DTYPE_CODE[Q.dtype], _ptr(argmax),
+                                _ptr(dS), _ptr(dD), _stream(stream))
+    _check(st, "maxsim_backward_dd")
+    return dD
 
 
 # ------------------------------------------------------------ sharded backward

@@ -250,29 +250,58 @@ size_t maxsim_backward_workspace_size(int n_queries, int nq, int d, int64_t B, i
   return backward_workspace_bytes(n_queries, nq, d, B);  // per-range dQ partials
 }
 
-maxsim_status maxsim_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
-                              const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
-                              float* dQ, float* dD, void* workspace, size_t workspace_bytes, void* stream) {
+// Shared checks of the three backward entry points; `parts` says which
+// gradients are computed, and only their inputs and outputs are checked.
+static maxsim_status backward_common(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                                     const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax,
+                                     const float* dS, float* dQ, float* dD, void* workspace, size_t workspace_bytes,
+                                     int parts, void* stream) {
+  const bool want_dd = parts & kBackwardDD, want_dq = parts & kBackwardDQ;
   if (n_queries < 1 || nq < 1 || d < 1 || B < 0 || nd < 1) return MAXSIM_ERR_INVALID_ARG;
   if (dtype != MAXSIM_BF16 && dtype != MAXSIM_FP16) return dtype == MAXSIM_FP32 ? MAXSIM_ERR_UNSUPPORTED
                                                                                : MAXSIM_ERR_INVALID_ARG;
   if (d % 64 != 0 || d > 1024 || static_cast<int64_t>(n_queries) * nq > 65536 || nd > 65535)
     return MAXSIM_ERR_UNSUPPORTED;
-  if (!Q || !dQ) return MAXSIM_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(dQ)) return MAXSIM_ERR_INVALID_ARG;
+  if ((want_dd && !Q) || (want_dq && !dQ)) return MAXSIM_ERR_INVALID_ARG;
+  if ((want_dd && !aligned16(Q)) || (want_dq && !aligned16(dQ))) return MAXSIM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (B == 0) {  // no documents: dQ is all zeros
+  if (B == 0) {  // no documents: dQ is all zeros, dD is empty
+    if (!want_dq) return MAXSIM_OK;
     return cudaMemsetAsync(dQ, 0, static_cast<size_t>(n_queries) * nq * d * sizeof(float), s) == cudaSuccess
                ? MAXSIM_OK
                : MAXSIM_ERR_CUDA;
   }
-  if (!D || !argmax || !dS || !dD) return MAXSIM_ERR_INVALID_ARG;
-  if (!aligned16(D) || !aligned4(argmax) || !aligned4(dS) || !aligned16(dD) || (doc_len && !aligned4(doc_len)))
+  if (!argmax || !dS || (want_dd && !dD) || (want_dq && !D)) return MAXSIM_ERR_INVALID_ARG;
+  if (!aligned4(argmax) || !aligned4(dS) || (want_dd && !aligned16(dD)) || (want_dq && !aligned16(D)) ||
+      (doc_len && !aligned4(doc_len)))
     return MAXSIM_ERR_INVALID_ARG;
-  const size_t need = backward_workspace_bytes(n_queries, nq, d, B);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return MAXSIM_ERR_WORKSPACE;
+  if (want_dq) {
+    const size_t need = backward_workspace_bytes(n_queries, nq, d, B);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return MAXSIM_ERR_WORKSPACE;
+  }
   return launch_backward(Q, n_queries, nq, d, D, B, nd, doc_len, dtype == MAXSIM_BF16 ? 1 : 0, argmax, dS, dQ, dD,
-                         static_cast<float*>(workspace), s);
+                         static_cast<float*>(workspace), parts, s);
+}
+
+maxsim_status maxsim_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                              const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
+                              float* dQ, float* dD, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_common(Q, n_queries, nq, d, D, B, nd, doc_len, dtype, argmax, dS, dQ, dD, workspace,
+                         workspace_bytes, kBackwardDD | kBackwardDQ, stream);
+}
+
+maxsim_status maxsim_backward_dq(int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                                 const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
+                                 float* dQ, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_common(nullptr, n_queries, nq, d, D, B, nd, doc_len, dtype, argmax, dS, dQ, nullptr, workspace,
+                         workspace_bytes, kBackwardDQ, stream);
+}
+
+maxsim_status maxsim_backward_dd(const void* Q, int n_queries, int nq, int d, int64_t B, int nd,
+                                 const int32_t* doc_len, maxsim_dtype dtype, const int32_t* argmax, const float* dS,
+                                 float* dD, void* stream) {
+  return backward_common(Q, n_queries, nq, d, nullptr, B, nd, doc_len, dtype, argmax, dS, nullptr, dD, nullptr, 0,
+                         kBackwardDD, stream);
 }
 
 }  // extern "C"

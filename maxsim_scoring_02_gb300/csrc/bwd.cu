@@ -17,17 +17,18 @@
 // writes the row -- every row of dD[b] is written by exactly one warp, rows
 // nothing points at as zeros.
 //
-// dq_kernel -- each CTA owns a block of (q, i) destination rows with fp32
-// accumulators in registers and sweeps one contiguous range of documents in
-// ascending order. A producer warp reads each document's argmax slice and
-// gathers the selected D rows into a shared-memory stage with one bulk copy
-// per row (cp.async.bulk, completing on the stage's mbarrier), several
-// documents ahead of the eight consumer warps, so the dependent argmax ->
-// row loads never stall the accumulation. The CTAs of a range sweep in the
-// same order, so the gathered rows are re-served from L2. With several
-// ranges each writes its own partial dQ to the workspace and
-// dq_reduce_kernel adds them in range order -- still destination-owned,
-// atomic-free and deterministic.
+// dq_kernel -- each CTA owns a block of (q, i) destination rows; a thread
+// holds 32 dimensions of one row as fp32 accumulators in registers and sweeps
+// one contiguous range of documents in ascending order. Per document it
+// copies its 64-byte slice of the selected D row into its own shared-memory
+// slot with 16-byte cp.async, several documents ahead of the one it
+// accumulates, and fetches the argmax entries and dS values further ahead
+// into a register ring, so the dependent argmax -> row loads never stall the
+// accumulation (no data is shared between threads, so no barrier is needed).
+// The CTAs of a range sweep in the same order, so the gathered rows are
+// re-served from L2. With several ranges each writes its own partial dQ to
+// the workspace and dq_reduce_kernel adds them in range order -- still
+// destination-owned, atomic-free and deterministic.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -360,8 +361,7 @@ __global__ void dq_reduce_kernel(const BwdParams p) {
 }
 
 template <typename T>
-maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream_t stream) {
-  // dD
+maxsim_status launch_dd(const BwdParams& p, const DeviceInfo* dev, cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>(p.nd) + 1 + p.nQ + kBwdWarps) * 4 +
                       (static_cast<size_t>(kBwdWarps) * p.nd + 2 * static_cast<size_t>(p.nQ) * p.nq) * 2;
   if (smem > static_cast<size_t>(dev->max_smem_optin)) return MAXSIM_ERR_UNSUPPORTED;
@@ -380,11 +380,15 @@ maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream
     default: return MAXSIM_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
-  // dQ
+  return MAXSIM_OK;
+}
+
+template <typename T>
+maxsim_status launch_dq(const BwdParams& p, cudaStream_t stream) {
   const int R = dq_rows(p.d);
   const int blocks = p.nQ * ((p.nq + R - 1) / R);
   const size_t dq_smem = dq_smem_bytes();
-  e = cudaFuncSetAttribute(dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dq_smem));
+  cudaError_t e = cudaFuncSetAttribute(dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dq_smem));
   if (e == cudaSuccess) dq_kernel<T><<<dim3(blocks, p.splits), kDqThreads, dq_smem, stream>>>(p);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
   if (p.splits > 1) {
@@ -394,6 +398,15 @@ maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, cudaStream
     if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
   }
   return MAXSIM_OK;
+}
+
+template <typename T>
+maxsim_status launch_typed(const BwdParams& p, const DeviceInfo* dev, int parts, cudaStream_t stream) {
+  if (parts & kBackwardDD) {
+    const maxsim_status st = launch_dd<T>(p, dev, stream);
+    if (st != MAXSIM_OK) return st;
+  }
+  return (parts & kBackwardDQ) ? launch_dq<T>(p, stream) : MAXSIM_OK;
 }
 
 }  // namespace
@@ -410,7 +423,7 @@ size_t backward_workspace_bytes(int n_queries, int nq, int d, int64_t B) {
 
 maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
                               const int32_t* doc_len, int is_bf16, const int32_t* argmax, const float* dS, float* dQ,
-                              float* dD, float* workspace, cudaStream_t stream) {
+                              float* dD, float* workspace, int parts, cudaStream_t stream) {
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
   BwdParams p;
@@ -430,7 +443,7 @@ maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const
   p.splits = backward_splits(B);
   p.partial = workspace;
   p.status = dev->status;
-  return is_bf16 ? launch_typed<__nv_bfloat16>(p, dev, stream) : launch_typed<__half>(p, dev, stream);
+  return is_bf16 ? launch_typed<__nv_bfloat16>(p, dev, parts, stream) : launch_typed<__half>(p, dev, parts, stream);
 }
 
 }  // namespace msim

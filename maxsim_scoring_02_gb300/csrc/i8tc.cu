@@ -146,7 +146,13 @@ __device__ __forceinline__ void i8tc_range(const I8TcParams& p, int64_t& b0, int
 
 // Four int8 (as biased bytes u = x + 128 in `xb`) -> two fp16x2 words holding
 // x exactly: PRMT puts each byte under the fp16 exponent byte 0x64 (value
-// 1024 + u), then one packed subtract of 1152.
+// 1024 + u), then one packed subtract of 1152. This is the standard
+// exponent-bias ("magic number") integer-to-float conversion: fp16 numbers in
+// [1024, 2048) have a spacing of exactly 1, so their low 10 mantissa bits are
+// an unsigned integer u < 1024 added to 1024; 0x6400 is 1024.0 and 0x6480 is
+// 1152.0 = 1024 + 128, so the subtract removes both the exponent bias and the
+// +128 byte bias with no rounding (every operand and result is an integer of
+// magnitude < 2048).
 __device__ __forceinline__ uint32_t h2_of(uint32_t xb, uint32_t sel) {
   uint32_t r, o;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(xb), "r"(0x64646464u), "r"(sel));

@@ -64,11 +64,15 @@ maxsim_status launch_streamed(const void* Q, int n_queries, int nq, int d, const
                               const int32_t* doc_len_host, int dtype, float* out, int32_t* argmax, void* workspace,
                               size_t workspace_bytes, int64_t chunk, cudaStream_t stream);
 
-// Backward through the saved argmax: dD (inverse CSR, destination-owned) and dQ.
+// Backward through the saved argmax: dD (inverse CSR, destination-owned) and
+// dQ. `parts` selects the gradients to compute (kBackwardDD | kBackwardDQ);
+// the pointers of a part not selected are not read.
+constexpr int kBackwardDD = 1;
+constexpr int kBackwardDQ = 2;
 size_t backward_workspace_bytes(int n_queries, int nq, int d, int64_t B);
 maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
                               const int32_t* doc_len, int is_bf16, const int32_t* argmax, const float* dS, float* dQ,
-                              float* dD, float* workspace, cudaStream_t stream);
+                              float* dD, float* workspace, int parts, cudaStream_t stream);
 
 // Encodes a TMA tensor map through the driver entry point (no libcuda link).
 // dtype_code: 0 fp16, 1 bf16, 2 uint8, 3 fp32; swizzle: 0 none, 1 128-byte,

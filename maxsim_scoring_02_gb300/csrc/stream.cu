@@ -3,7 +3,8 @@
 // reading §5). Host-side runtime only: the documents are copied in chunks
 // into two device buffers that alternate, the copy of chunk k + 1 running on
 // a library-owned copy stream while chunk k is scored on the caller's
-// stream; events order each buffer's reuse. Every chunk is scored by the
+// stream; events order each buffer's reuse, and the copy stream first waits
+// for the work already queued on the caller's stream. Every chunk is scored by the
 // same forward kernels as maxsim_score, so the per-document results are the
 // same as scoring the whole corpus from device memory.
 #include <cuda_runtime.h>
@@ -72,12 +73,19 @@ maxsim_status launch_streamed(const void* Q, int n_queries, int nq, int d, const
   float* otmp = reinterpret_cast<float*>(ws + 2 * (l.dbuf + l.lbuf));
   int32_t* atmp = reinterpret_cast<int32_t*>(ws + 2 * (l.dbuf + l.lbuf) + l.obuf);
 
-  cudaEvent_t copied[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr};
+  cudaEvent_t copied[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr}, entry = nullptr;
   maxsim_status st = MAXSIM_OK;
   for (int i = 0; i < 2 && st == MAXSIM_OK; ++i)
     if (cudaEventCreateWithFlags(&copied[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&consumed[i], cudaEventDisableTiming) != cudaSuccess)
       st = MAXSIM_ERR_CUDA;
+  // The copy stream starts after everything already queued on the caller's
+  // stream: an earlier call's kernels may still be reading the workspace
+  // buffers the first two chunks are about to overwrite.
+  if (st == MAXSIM_OK && (cudaEventCreateWithFlags(&entry, cudaEventDisableTiming) != cudaSuccess ||
+                          cudaEventRecord(entry, stream) != cudaSuccess ||
+                          cudaStreamWaitEvent(cs, entry, 0) != cudaSuccess))
+    st = MAXSIM_ERR_CUDA;
   const size_t doc_bytes = static_cast<size_t>(nd) * d * esz;
   const int64_t n_chunks = (B + chunk - 1) / chunk;
   for (int64_t k = 0; k < n_chunks && st == MAXSIM_OK; ++k) {
@@ -121,6 +129,7 @@ maxsim_status launch_streamed(const void* Q, int n_queries, int nq, int d, const
     if (copied[i]) cudaEventDestroy(copied[i]);
     if (consumed[i]) cudaEventDestroy(consumed[i]);
   }
+  if (entry) cudaEventDestroy(entry);
   return st;
 }
 

@@ -90,3 +90,19 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "maxsim_oracle" not in text, f
+
+
+def test_backward_halves_validate_before_launch(lib):
+    """dQ-only and dD-only backward entry points: missing inputs or outputs,
+    fp32 inputs and a missing dQ workspace are rejected on the host."""
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # dD only: Q missing / dD missing / fp32 unsupported
+    assert lib.maxsim_backward_dd(None, 1, 32, 128, 10, 64, None, 0, fake, fake, fake, None) == 1
+    assert lib.maxsim_backward_dd(fake, 1, 32, 128, 10, 64, None, 0, fake, fake, None, None) == 1
+    assert lib.maxsim_backward_dd(fake, 1, 32, 128, 10, 64, None, 2, fake, fake, fake, None) == 2
+    # dQ only: D missing / dQ missing / workspace missing when the range split needs one
+    assert lib.maxsim_backward_dq(1, 32, 128, None, 10, 64, None, 0, fake, fake, fake, None, 0, None) == 1
+    assert lib.maxsim_backward_dq(1, 32, 128, fake, 10, 64, None, 0, fake, fake, None, None, 0, None) == 1
+    assert m.maxsim_backward_workspace_size(1, 32, 128, 5000, 64) > 0
+    assert lib.maxsim_backward_dq(1, 32, 128, fake, 5000, 64, None, 0, fake, fake, fake, None, 0, None) == 5

@@ -137,3 +137,81 @@ def test_backward_split_document_ranges():
     dS = workloads.normal((nQ, B), seed=604)
     assert m.maxsim_backward_workspace_size(nQ, nq, d, B, nd) > 0
     _run(Q, D, L, dS)
+
+
+def test_backward_halves_equal_full_call():
+    """maxsim_backward_dq and maxsim_backward_dd run the same kernels as the
+    two halves of maxsim_backward: their outputs are identical to it."""
+    nQ, nq, B, nd, d = 2, 48, 2500, 90, 128
+    Q = workloads.normalized_tokens((nQ, nq, d), seed=701, dtype="bf16").to(DEV)
+    D = workloads.normalized_tokens((B, nd, d), seed=702, dtype="bf16").to(DEV)
+    L = workloads.uniform_lengths(B, 0, nd, seed=703).to(DEV)
+    dS = workloads.normal((nQ, B), seed=704).to(DEV)
+    _, am = m.maxsim_score(Q, D, L, want_argmax=True)
+    dQ, dD = m.maxsim_backward(Q, D, am, dS, doc_len=L)
+    dQ1 = m.maxsim_backward_dq(D, am, dS, doc_len=L)
+    dD1 = m.maxsim_backward_dd(Q, am, dS, nd, doc_len=L)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    assert torch.equal(dQ1, dQ) and torch.equal(dD1, dD)
+
+
+def _allreduce_worker(rank, world, port, part, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = torch.from_numpy(part)
+    m.allreduce_dq(t)
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, t.numpy()))
+
+
+def test_document_sharded_backward_sums_to_full_gradient():
+    """Data-parallel sharding of the training step (TileMaxSim deep reading
+    §5): each shard runs maxsim_backward on its own documents, with its slice
+    of the forward argmax and of dS. The shards' dQ partials, summed as
+    allreduce_dq sums them (here through a two-rank gloo group on host
+    copies), equal the oracle's dQ over the whole batch, and every shard's
+    dD equals the oracle's dD rows of its documents. The shards are uneven,
+    so one runs the range-split dQ sweep (B >= 2048) and one does not."""
+    import socket
+    import torch.multiprocessing as mp
+    nQ, nq, nd, d = 3, 40, 70, 128
+    cuts = [0, 1900, 4200]
+    B = cuts[-1]
+    Q = workloads.normalized_tokens((nQ, nq, d), seed=801, dtype="bf16")
+    D = workloads.normalized_tokens((B, nd, d), seed=802, dtype="bf16")
+    L = workloads.uniform_lengths(B, 0, nd, seed=803)
+    dS = workloads.normal((nQ, B), seed=804)
+    Qd, Dd, Ld, dSd = Q.to(DEV), D.to(DEV), L.to(DEV), dS.to(DEV)
+    _, am = m.maxsim_score(Qd, Dd, Ld, want_argmax=True)
+    parts, dDs = [], []
+    for b0, b1 in zip(cuts[:-1], cuts[1:]):
+        dQp, dDp = m.maxsim_backward(Qd, Dd[b0:b1], am[:, b0:b1].contiguous(), dSd[:, b0:b1].contiguous(),
+                                     doc_len=Ld[b0:b1])
+        parts.append(dQp.cpu().numpy().astype(np.float64))
+        dDs.append(dDp)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    rQ, rD = oracle.backward(_np(Q), _np(D), am.cpu().numpy(), dS.double().numpy(), L.numpy())
+    assert _rel(parts[0] + parts[1], rQ) <= REL
+    for (b0, b1), dDp in zip(zip(cuts[:-1], cuts[1:]), dDs):
+        assert _rel(dDp.cpu().numpy(), rD[b0:b1]) <= REL
+    # the same sum through the library's all-reduce on a two-rank gloo group
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    qu = ctx.Queue()
+    procs = [ctx.Process(target=_allreduce_worker, args=(r, 2, port, parts[r], qu)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(qu.get(timeout=180) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(2):
+        np.testing.assert_array_equal(res[r], parts[0] + parts[1])
+        assert _rel(res[r], rQ) <= REL

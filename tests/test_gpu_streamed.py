@@ -66,3 +66,28 @@ def test_streamed_short_workspace_is_rejected():
     ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
     with pytest.raises(m.MaxSimError):
         m.maxsim_score_streamed(Q, D, chunk_docs=32, workspace=ws)
+
+
+def test_back_to_back_calls_share_one_workspace():
+    """Two streamed calls queued back to back on one stream and one workspace,
+    with different documents and no synchronisation between them: the second
+    call's first copies must wait for the first call's kernels still reading
+    the same buffers. Each result equals device-resident scoring exactly."""
+    B, nd, d, chunk = 12_000, 128, 128, 4096
+    Q = workloads.normalized_tokens((32, d), seed=81, dtype="bf16").to(DEV)
+    D1 = workloads.normalized_tokens((B, nd, d), seed=82, dtype="bf16")
+    D2 = workloads.normalized_tokens((B, nd, d), seed=83, dtype="bf16")
+    L2 = workloads.uniform_lengths(B, 1, nd, seed=84)
+    nb = m.maxsim_score_streamed_workspace_size(1, 32, nd, d, torch.bfloat16, chunk)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    h1, h2, hl2 = D1.pin_memory(), D2.pin_memory(), L2.pin_memory()
+    ref1 = m.maxsim_score(Q, D1.to(DEV))
+    ref2 = m.maxsim_score(Q, D2.to(DEV), L2.to(DEV))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        out1 = m.maxsim_score_streamed(Q, h1, None, chunk_docs=chunk, workspace=ws)
+        out2 = m.maxsim_score_streamed(Q, h2, hl2, chunk_docs=chunk, workspace=ws)
+        torch.cuda.synchronize()
+        assert m.maxsim_device_status() == (0, 0)
+        assert torch.equal(out1, ref1)
+        assert torch.equal(out2, ref2)
