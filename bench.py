@@ -183,6 +183,14 @@ class Headline:
             self.L = w.uniform_lengths(self.B, 32, self.nd, seed=seed + 2, device=device)
             w.zero_padding(self.D, self.L)
         self.out = torch.empty((1, self.B), dtype=torch.float32, device=device)
+        self.order = None
+        if getattr(args, "order", "index") == "length" and torch.device(device).type == "cuda":
+            # length-bucketed walk: depends only on the lengths, computed once per corpus (not timed per step)
+            L = self.L if self.L is not None else torch.full((self.B,), self.nd, dtype=torch.int32, device=device)
+            t0 = time.perf_counter()
+            self.order = m.maxsim_length_order(doc_len=L, nd=self.nd)
+            torch.cuda.synchronize()
+            self.order_ms = 1e3 * (time.perf_counter() - t0)
         self.bound = "hbm"
         if self.dtype == "fp32":
             # 16 FLOP per document byte against a ~12 FLOP/B FP32 ridge: the FMA pipe bounds it
@@ -201,11 +209,19 @@ class Headline:
                        "doc_lengths": "U{32..%d} zero-padded, masked" % self.nd if self.lenmask else "full",
                        "inputs": "L2-normalised N(0,1) tokens, seeded",
                        "l2": "inputs (%.2f GB) larger than L2 (129 MB); no flush" % (self.D.numel() * esz / 1e9)}
+        if self.order is not None:
+            self.workload += "_length_ordered"
+            self.config.update(workload=self.workload,
+                               doc_order="length-bucketed (maxsim_length_order once per corpus: %.2f ms host-timed, "
+                                         "outside the timed steps)" % self.order_ms)
 
     def step(self, ev=None):
         if ev is not None:
             ev[0].record()
-        self.m.maxsim_score(self.Q, self.D, self.L, out=self.out)
+        if self.order is not None:
+            self.m.maxsim_score_ordered(self.Q, self.D, self.order, self.L, out=self.out)
+        else:
+            self.m.maxsim_score(self.Q, self.D, self.L, out=self.out)
         if ev is not None:
             ev[1].record()
 
@@ -557,8 +573,95 @@ class ColPaliTrain:
         return run, n
 
 
+class Footprint:
+    """Memory footprint of the fused path against a materialising one
+    (FLASH-MAXSIM Abstract: memory savings; review page Fig. 2: the batch
+    sizes at which materialising implementations run out of memory).
+
+    For a sweep of ColPali-shaped batches (16 queries x 1024 tokens against B
+    documents of 1024 tokens, d = 128, bf16) it measures the peak device
+    bytes of the fused inference call (scores) and of the fused training step
+    (scores + argmax, then dD and dQ), from torch's allocator: every buffer
+    the library touches is a caller-owned torch tensor. Beside each it puts
+    the bytes a materialising implementation would need on top of the same
+    inputs and outputs -- the similarity tensor S[nQ,B,Lq,Ld] in fp32, and
+    for training also its gradient -- and, from the device's capacity, the
+    batch size at which that alone no longer fits. No materialising
+    implementation is run: its extra bytes follow from the shapes."""
+    kernel = "fwd_qm"
+    kernel_files = ("fwd_qm.cu", "ptx.cuh")
+    bound = "tensor"
+    SWEEP = (1000, 2000, 5000, 10000, 20000, 40000)
+
+    def __init__(self, args, device, rank):
+        import maxsim_scoring_02_gb300 as m
+        self.m, self.device = m, device
+        self.nQ, self.nq, self.nd, self.d = 16, 1024, 1024, 128
+        self.workload = f"footprint_colpali_q{self.nQ}x{self.nq}_nd{self.nd}_d{self.d}_bf16"
+
+    def measure(self):
+        import workloads as w
+        dev = self.device
+        cap = torch.cuda.get_device_properties(dev).total_memory
+        rows = []
+        for B in self.SWEEP:
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
+            Q = w.normalized_tokens((self.nQ, self.nq, self.d), seed=B, dtype="bf16", device=dev)
+            D = w.normalized_tokens((B, self.nd, self.d), seed=B + 1, dtype="bf16", device=dev)
+            torch.cuda.synchronize(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            base = torch.cuda.memory_allocated(dev)
+            out = self.m.maxsim_score(Q, D)
+            torch.cuda.synchronize(dev)
+            inf_peak = torch.cuda.max_memory_allocated(dev)
+            del out
+            torch.cuda.reset_peak_memory_stats(dev)
+            dS = w.normal((self.nQ, B), seed=B + 2, device=dev)
+            out, am = self.m.maxsim_score(Q, D, want_argmax=True)
+            dQ, dD = self.m.maxsim_backward(Q, D, am, dS)
+            torch.cuda.synchronize(dev)
+            st, flags = self.m.maxsim_device_status()
+            if st != 0:
+                raise SystemExit(f"device status in footprint sweep: {st} flags {flags}")
+            train_peak = torch.cuda.max_memory_allocated(dev)
+            del Q, D, dS, out, am, dQ, dD
+            sim = 4 * self.nQ * B * self.nq * self.nd
+            rows.append({"B": B, "inputs_bytes": int(base),
+                         "fused_inference_peak_bytes": int(inf_peak), "fused_training_peak_bytes": int(train_peak),
+                         "materialising_inference_bytes": int(inf_peak + sim),
+                         "materialising_training_bytes": int(train_peak + 2 * sim),
+                         "ratio_inference": (inf_peak + sim) / inf_peak,
+                         "ratio_training": (train_peak + 2 * sim) / train_peak})
+        torch.cuda.empty_cache()
+        # largest batch that fits the device: fused (linear fit of the measured peaks per document)
+        # against materialising (S alone, and S plus its gradient)
+        per_doc_inf = (rows[-1]["fused_inference_peak_bytes"] - rows[0]["fused_inference_peak_bytes"]) / (
+            rows[-1]["B"] - rows[0]["B"])
+        per_doc_train = (rows[-1]["fused_training_peak_bytes"] - rows[0]["fused_training_peak_bytes"]) / (
+            rows[-1]["B"] - rows[0]["B"])
+        sim_per_doc = 4 * self.nQ * self.nq * self.nd
+        return {"device_bytes": int(cap), "sweep": rows,
+                "max_B_fused_inference": int(cap / per_doc_inf),
+                "max_B_fused_training": int(cap / per_doc_train),
+                "max_B_materialising_inference": int(cap / (per_doc_inf + sim_per_doc)),
+                "max_B_materialising_training": int(cap / (per_doc_train + 2 * sim_per_doc))}
+
+
+def run_footprint(args, device):
+    wl = Footprint(args, device, 0)
+    res = wl.measure()
+    line = {"metric": "peak device bytes of the fused MaxSim path against a materialising one",
+            "value": res["sweep"][-1]["fused_training_peak_bytes"], "unit": "bytes", "n_gpus": 1,
+            "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.workload, "queries": wl.nQ, "Lq": wl.nq, "Ld": wl.nd, "d": wl.d,
+                       "B_sweep": list(wl.SWEEP), "value": "fused training-step peak at the largest B"},
+            "footprint": res}
+    print(json.dumps(line), flush=True)
+
+
 WORKLOADS = {"colbert_full": Headline, "colbert_lenmask": Headline, "varlen": Varlen, "pq": PQ, "i8": I8,
-             "colpali_train": ColPaliTrain}
+             "colpali_train": ColPaliTrain, "footprint": Footprint}
 
 
 # ------------------------------------------------------------------- main
@@ -574,6 +677,8 @@ def parse():
     ap.add_argument("--B", type=int, default=100_000)
     ap.add_argument("--nd", type=int, default=128)
     ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--order", default="index", choices=["index", "length"],
+                    help="padded workloads: walk documents in index order or length-bucketed order")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
@@ -644,6 +749,10 @@ def run_reference(args, world, rank):
     """The oracle on the host cores, on the same config, steps of a bounded sample."""
     if rank != 0:
         return
+    if args.workload == "footprint":
+        print(json.dumps({"impl": "reference", "unavailable": "the footprint sweep measures device memory only; "
+                          "the oracle arm has no device footprint"}), flush=True)
+        return
     import copy
 
     import oracle
@@ -686,6 +795,10 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     peaks = load_peaks()
+    if args.workload == "footprint":
+        if rank == 0:
+            run_footprint(args, device)
+        return
     wl = WORKLOADS[args.workload](args, device, rank)
     stream = torch.cuda.current_stream()
 

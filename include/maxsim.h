@@ -71,6 +71,25 @@ typedef enum maxsim_dtype {
 #define MAXSIM_DEVERR_TIMEOUT    0x1u  /* a pipeline wait exceeded its time bound */
 #define MAXSIM_DEVERR_BAD_INPUT  0x2u  /* a document's offsets/length were out of range */
 
+/*
+ * maxsim_debug_set_faults -- TEST-ONLY switches of the failure-detection
+ * path; not part of the operator, never needed in normal use. Applies to the
+ * current device, to every kernel launched after the call returns (the call
+ * is synchronous).
+ *   flags          MAXSIM_DEBUG_STALL_FWD_LOADER: the loader role of the
+ *                  tensor-core forward kernel (maxsim_score / _varlen with
+ *                  bf16 or fp16 and queries below 256 tokens) issues no copy,
+ *                  so the kernel's other roles wait on barriers nothing will
+ *                  complete; their bounded waits run out, record
+ *                  MAXSIM_DEVERR_TIMEOUT and the kernel exits with no copy or
+ *                  MMA in flight (its outputs are then undefined). 0 = off.
+ *   wait_limit_ns  bound of every pipeline wait; 0 restores the default (2 s).
+ * Call maxsim_debug_set_faults(0, 0) to return to normal operation. Unknown
+ * flag bits return MAXSIM_ERR_INVALID_ARG; a failed copy MAXSIM_ERR_CUDA.
+ */
+#define MAXSIM_DEBUG_STALL_FWD_LOADER 0x1u
+maxsim_status maxsim_debug_set_faults(unsigned int flags, uint64_t wait_limit_ns);
+
 /* Library version: major*10000 + minor*100 + patch. */
 int maxsim_version(void);
 
@@ -112,6 +131,43 @@ maxsim_status maxsim_score(const void *Q, int n_queries, int nq, int d,
                            const void *D, int64_t B, int nd, const int32_t *doc_len,
                            maxsim_dtype dtype, float *out, int32_t *argmax_out,
                            void *stream);
+
+/*
+ * maxsim_length_order -- length-bucketed document order (TileMaxSim §5:
+ * fixed-Nd padding wastes token compute on variable-length corpora, and
+ * batching documents of similar length recovers the throughput). Writes the
+ * permutation order_out[B] that sorts the documents by their number of 8-row
+ * granules, ceil(L_b / 8), ascending and stably (equal keys keep index
+ * order). It depends only on the lengths: compute it once per corpus and
+ * pass it to maxsim_score_ordered for every query.
+ *   doc_len    [B] int32, 0 <= L_b <= nd (padded layout), or
+ *   offsets    [B+1] int64 (CSR layout; nd ignored, lengths above 8176
+ *              tokens share the last bucket) -- exactly one of the two, or
+ *              neither (every document has nd tokens: the identity order)
+ *   workspace  >= maxsim_length_order_workspace_size(B, nd, csr) bytes,
+ *              16-byte aligned (per-warp bucket counts)
+ * A length outside [0, nd] (or a decreasing offset) counts as 0 and sets
+ * MAXSIM_DEVERR_BAD_INPUT. B <= INT32_MAX.
+ */
+size_t maxsim_length_order_workspace_size(int64_t B, int nd, int csr);
+maxsim_status maxsim_length_order(const int32_t *doc_len, const int64_t *offsets, int64_t B, int nd,
+                                  int32_t *order_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * maxsim_score_ordered -- maxsim_score with the documents walked in the order
+ * doc_order (a permutation of [0, B), e.g. from maxsim_length_order), so each
+ * thread block scores documents of similar length. Results are written at
+ * the documents' own indices and are identical to maxsim_score's: a
+ * document's result depends only on its own rows. An entry outside [0, B)
+ * is skipped and sets MAXSIM_DEVERR_BAD_INPUT; duplicates leave the missing
+ * documents' outputs unwritten. Same arguments and limits as maxsim_score,
+ * bf16/fp16 only, and queries shorter than 256 tokens (longer ones, and fp32,
+ * return MAXSIM_ERR_UNSUPPORTED).
+ */
+maxsim_status maxsim_score_ordered(const void *Q, int n_queries, int nq, int d,
+                                   const void *D, int64_t B, int nd, const int32_t *doc_len,
+                                   const int32_t *doc_order, maxsim_dtype dtype, float *out,
+                                   int32_t *argmax_out, void *stream);
 
 /*
  * maxsim_score_varlen -- variable-length, padding-free documents in CSR

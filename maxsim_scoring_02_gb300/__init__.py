@@ -19,7 +19,8 @@ import os
 import torch
 
 __all__ = [
-    "MaxSimError", "library_path", "load_library", "maxsim_score", "maxsim_score_varlen",
+    "MaxSimError", "library_path", "load_library", "maxsim_score", "maxsim_score_varlen", "maxsim_length_order",
+    "maxsim_score_ordered", "maxsim_length_order_workspace_size",
     "maxsim_score_streamed", "maxsim_score_streamed_workspace_size",
     "maxsim_score_pq", "maxsim_score_pq_workspace_size", "maxsim_score_i8", "maxsim_backward",
     "maxsim_backward_workspace_size", "maxsim_backward_dq", "maxsim_backward_dd", "maxsim_device_status",
@@ -36,11 +37,14 @@ STATUS_NAMES = {0: "MAXSIM_OK", 1: "MAXSIM_ERR_INVALID_ARG", 2: "MAXSIM_ERR_UNSU
                 3: "MAXSIM_ERR_CUDA", 4: "MAXSIM_ERR_TIMEOUT", 5: "MAXSIM_ERR_WORKSPACE"}
 DEVERR_TIMEOUT = 0x1
 DEVERR_BAD_INPUT = 0x2
+DEBUG_STALL_FWD_LOADER = 0x1
 
 # Every symbol the header declares (checked by the tests).
 EXPORTS = (
-    "maxsim_version", "maxsim_status_string", "maxsim_device_status", "maxsim_score",
-    "maxsim_score_varlen", "maxsim_score_streamed_workspace_size", "maxsim_score_streamed",
+    "maxsim_version", "maxsim_status_string", "maxsim_device_status", "maxsim_debug_set_faults",
+    "maxsim_score",
+    "maxsim_score_varlen", "maxsim_length_order_workspace_size", "maxsim_length_order", "maxsim_score_ordered",
+    "maxsim_score_streamed_workspace_size", "maxsim_score_streamed",
     "maxsim_score_pq_workspace_size", "maxsim_score_pq", "maxsim_score_pq_noalloc",
     "maxsim_score_i8",
     "maxsim_backward_workspace_size", "maxsim_backward", "maxsim_backward_dq", "maxsim_backward_dd",
@@ -76,8 +80,16 @@ def load_library():
     lib.maxsim_status_string.argtypes = [I32]
     lib.maxsim_device_status.restype = I32
     lib.maxsim_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+    lib.maxsim_debug_set_faults.restype = I32
+    lib.maxsim_debug_set_faults.argtypes = [ctypes.c_uint, ctypes.c_uint64]
     lib.maxsim_score.restype = I32
     lib.maxsim_score.argtypes = [P, I32, I32, I32, P, I64, I32, P, I32, P, P, P]
+    lib.maxsim_length_order_workspace_size.restype = SZ
+    lib.maxsim_length_order_workspace_size.argtypes = [I64, I32, I32]
+    lib.maxsim_length_order.restype = I32
+    lib.maxsim_length_order.argtypes = [P, P, I64, I32, P, P, SZ, P]
+    lib.maxsim_score_ordered.restype = I32
+    lib.maxsim_score_ordered.argtypes = [P, I32, I32, I32, P, I64, I32, P, P, I32, P, P, P]
     lib.maxsim_score_varlen.restype = I32
     lib.maxsim_score_varlen.argtypes = [P, I32, I32, I32, P, P, I64, I64, I32, P, P, P]
     lib.maxsim_score_streamed_workspace_size.restype = SZ
@@ -169,6 +181,66 @@ def maxsim_score(Q, D, doc_len=None, out=None, argmax_out=None, want_argmax=Fals
     st = lib.maxsim_score(_ptr(Q3), nQ, nq, d, _ptr(D), B, nd, _ptr(doc_len), _DTYPE_CODE[Q.dtype],
                           _ptr(out), _ptr(argmax_out), _stream(stream))
     _check(st, "maxsim_score")
+    return (out, argmax_out) if argmax_out is not None else out
+
+
+def maxsim_length_order_workspace_size(B, nd, csr=False):
+    """Device bytes of the workspace of maxsim_length_order (no GPU needed)."""
+    return int(load_library().maxsim_length_order_workspace_size(B, nd, 1 if csr else 0))
+
+
+def maxsim_length_order(doc_len=None, offsets=None, B=None, nd=None, order=None, stream=None):
+    """Length-bucketed document order: int32 [B] permutation sorting documents
+    by ceil(L_b / 8), ascending and stable. Give doc_len [B] int32 with nd
+    (padded layout) or offsets [B+1] int64 (CSR)."""
+    lib = load_library()
+    if (doc_len is None) == (offsets is None):
+        raise ValueError("give exactly one of doc_len and offsets")
+    ref = doc_len if doc_len is not None else offsets
+    if doc_len is not None:
+        _dev(doc_len, "doc_len", torch.int32)
+        B = doc_len.numel()
+        if nd is None:
+            raise ValueError("nd is required with doc_len")
+    else:
+        _dev(offsets, "offsets", torch.int64)
+        B = offsets.numel() - 1
+        nd = 0
+    if order is None:
+        order = torch.empty(B, dtype=torch.int32, device=ref.device)
+    _dev(order, "order", torch.int32)
+    nb = lib.maxsim_length_order_workspace_size(B, nd, 0 if doc_len is not None else 1)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=ref.device)
+    st = lib.maxsim_length_order(_ptr(doc_len), _ptr(offsets), B, nd, _ptr(order), _ptr(ws), ws.numel(),
+                                 _stream(stream))
+    _check(st, "maxsim_length_order")
+    return order
+
+
+def maxsim_score_ordered(Q, D, doc_order, doc_len=None, out=None, argmax_out=None, want_argmax=False, stream=None):
+    """maxsim_score with the documents walked in doc_order (int32 [B]
+    permutation); results land at the documents' own indices."""
+    lib = load_library()
+    _dev(Q, "Q")
+    _dev(D, "D", Q.dtype)
+    _dev(doc_order, "doc_order", torch.int32)
+    Q3 = Q if Q.dim() == 3 else Q.unsqueeze(0)
+    nQ, nq, d = Q3.shape
+    B, nd, d2 = D.shape
+    if d2 != d or doc_order.numel() != B:
+        raise ValueError("Q, D and doc_order disagree")
+    if doc_len is not None:
+        _dev(doc_len, "doc_len", torch.int32)
+    if out is None:
+        out = torch.empty((nQ, B), dtype=torch.float32, device=Q.device)
+    _dev(out, "out", torch.float32)
+    if want_argmax and argmax_out is None:
+        argmax_out = torch.empty((nQ, B, nq), dtype=torch.int32, device=Q.device)
+    if argmax_out is not None:
+        _dev(argmax_out, "argmax_out", torch.int32)
+    st = lib.maxsim_score_ordered(_ptr(Q3), nQ, nq, d, _ptr(D), B, nd, _ptr(doc_len), _ptr(doc_order),
+                                  _DTYPE_CODE[Q.dtype], _ptr(out), _ptr(argmax_out), _stream(stream))
+    _check(st, "maxsim_score_ordered")
     return (out, argmax_out) if argmax_out is not None else out
 
 

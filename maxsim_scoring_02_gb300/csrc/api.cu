@@ -13,8 +13,11 @@
 
 namespace msim {
 
-// Per-device status word written by kernels (timeouts, bad documents).
-__device__ unsigned g_status_word;
+// Per-device status block: word 0 is the status word written by kernels
+// (timeouts, bad documents); word 1 holds test-only fault switches; words 2-3
+// the bound of pipeline waits in ns (0 = the default). Kernels receive its
+// address as their `status` pointer.
+__device__ __align__(16) unsigned g_status_block[4];
 
 namespace {
 
@@ -30,6 +33,9 @@ EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// CSR lengths are bucketed up to this many tokens (1023 8-row granules).
+constexpr int kOrderCsrNd = 8 * 1023;
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
@@ -44,9 +50,9 @@ const DeviceInfo* device_info() {
     if (cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return nullptr;
     void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_block) != cudaSuccess) return nullptr;
     info.status = static_cast<unsigned*>(addr);
-    if (cudaMemset(info.status, 0, sizeof(unsigned)) != cudaSuccess) return nullptr;
+    if (cudaMemset(info.status, 0, 4 * sizeof(unsigned)) != cudaSuccess) return nullptr;
     g_dev[dev] = info;
     g_dev_ready[dev] = true;
   }
@@ -124,6 +130,18 @@ maxsim_status maxsim_device_status(void* stream, unsigned int* flags) {
   return MAXSIM_OK;
 }
 
+maxsim_status maxsim_debug_set_faults(unsigned int flags, uint64_t wait_limit_ns) {
+  if (flags & ~static_cast<unsigned>(MAXSIM_DEBUG_STALL_FWD_LOADER)) return MAXSIM_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MAXSIM_ERR_CUDA;
+  const unsigned words[3] = {flags, static_cast<unsigned>(wait_limit_ns & 0xffffffffu),
+                             static_cast<unsigned>(wait_limit_ns >> 32)};
+  // synchronous: visible to every kernel launched after this call returns
+  if (cudaMemcpy(dev->status + 1, words, sizeof(words), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MAXSIM_ERR_CUDA;
+  return MAXSIM_OK;
+}
+
 static maxsim_status check_common(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B,
                                   maxsim_dtype dtype, const float* out, const int32_t* argmax_out) {
   if (n_queries < 1 || nq < 1 || d < 1 || B < 0) return MAXSIM_ERR_INVALID_ARG;
@@ -157,6 +175,37 @@ maxsim_status maxsim_score(const void* Q, int n_queries, int nq, int d, const vo
                           doc_len, nullptr, B, nd, out, argmax_out, s);
   return launch_fwd_tc(Q, n_queries, nq, d, D, rows, 0, doc_len, nullptr, B, nd, dtype == MAXSIM_BF16 ? 1 : 0, out,
                        argmax_out, s);
+}
+
+size_t maxsim_length_order_workspace_size(int64_t B, int nd, int csr) {
+  if (B < 0 || (!csr && nd < 1)) return 0;
+  return length_order_workspace_bytes(B, csr ? kOrderCsrNd : nd);
+}
+
+maxsim_status maxsim_length_order(const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
+                                  int32_t* order_out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || B > INT_MAX || (doc_len && offsets) || (!offsets && nd < 1)) return MAXSIM_ERR_INVALID_ARG;
+  if (B == 0) return MAXSIM_OK;
+  if (!order_out || !aligned4(order_out) || (doc_len && !aligned4(doc_len)) || (offsets && !aligned4(offsets)))
+    return MAXSIM_ERR_INVALID_ARG;
+  const int keys_nd = offsets ? kOrderCsrNd : nd;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < length_order_workspace_bytes(B, keys_nd))
+    return MAXSIM_ERR_WORKSPACE;
+  return launch_length_order(doc_len, offsets, B, keys_nd, order_out, workspace, static_cast<cudaStream_t>(stream));
+}
+
+maxsim_status maxsim_score_ordered(const void* Q, int n_queries, int nq, int d, const void* D, int64_t B, int nd,
+                                   const int32_t* doc_len, const int32_t* doc_order, maxsim_dtype dtype, float* out,
+                                   int32_t* argmax_out, void* stream) {
+  maxsim_status st = check_common(Q, n_queries, nq, d, D, B, dtype, out, argmax_out);
+  if (st != MAXSIM_OK) return st;
+  if (nd < 1 || (doc_len && !aligned4(doc_len))) return MAXSIM_ERR_INVALID_ARG;
+  if (B == 0) return MAXSIM_OK;
+  if (!doc_order || !aligned4(doc_order) || B > INT_MAX || B > INT64_MAX / nd) return MAXSIM_ERR_INVALID_ARG;
+  if (dtype == MAXSIM_FP32) return MAXSIM_ERR_UNSUPPORTED;
+  const int64_t rows = B * static_cast<int64_t>(nd);
+  return launch_fwd_tc(Q, n_queries, nq, d, D, rows, 0, doc_len, nullptr, B, nd, dtype == MAXSIM_BF16 ? 1 : 0, out,
+                       argmax_out, static_cast<cudaStream_t>(stream), doc_order);
 }
 
 size_t maxsim_score_streamed_workspace_size(int n_queries, int nq, int nd, int d, maxsim_dtype dtype,

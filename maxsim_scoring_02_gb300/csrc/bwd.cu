@@ -41,8 +41,6 @@
 namespace msim {
 namespace {
 
-constexpr int kBwdThreads = 256;
-constexpr int kBwdWarps = kBwdThreads / 32;
 
 // Two packed 16-bit values (low half first) as floats, exactly.
 template <typename T>
@@ -91,22 +89,62 @@ __device__ __forceinline__ int doc_length(const BwdParams& p, int64_t b) {
 }
 
 // ------------------------------------------------------------------- dD
-// DPL = d / 32 values per lane (2 per bf16x2 load).
-template <typename T, int DPL>
-__global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
+// NW warps per CTA. DPL = d / 32 values per lane: lane l owns the DPL
+// consecutive dimensions [DPL l, DPL l + DPL) of a row, so one warp load of a
+// Q row is d * 2 contiguous bytes (whole 32-byte sectors).
+
+// DPL 16-bit values at `src` (DPL * 2 bytes, aligned to that size up to 16)
+// as DPL / 2 packed 32-bit words.
+template <int DPL>
+__device__ __forceinline__ void load_row_words(const void* src, uint32_t (&w)[DPL / 2]) {
+  if constexpr (DPL % 8 == 0) {
+#pragma unroll
+    for (int c = 0; c < DPL / 8; ++c) {
+      const uint4 v = __ldg(static_cast<const uint4*>(src) + c);
+      w[4 * c] = v.x;
+      w[4 * c + 1] = v.y;
+      w[4 * c + 2] = v.z;
+      w[4 * c + 3] = v.w;
+    }
+  } else if constexpr (DPL % 4 == 0) {
+#pragma unroll
+    for (int c = 0; c < DPL / 4; ++c) {
+      const uint2 v = __ldg(static_cast<const uint2*>(src) + c);
+      w[2 * c] = v.x;
+      w[2 * c + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < DPL / 2; ++c) w[c] = __ldg(static_cast<const uint32_t*>(src) + c);
+  }
+}
+
+// Entries of one destination row gathered per batch: enough Q-row loads in
+// flight per lane to cover L2 latency, within the register budget.
+__host__ __device__ constexpr int dd_batch(int dpl) { return dpl <= 4 ? 8 : dpl <= 8 ? 4 : 2; }
+
+__host__ __device__ constexpr size_t dd_smem_bytes(int nw, int nd, int nQ, int ne) {
+  return (static_cast<size_t>(nd) + 1 + nQ + nw) * 4 + (static_cast<size_t>(nw) * nd + 2 * static_cast<size_t>(ne)) * 2;
+}
+
+template <typename T, int DPL, int NW>
+__global__ void __launch_bounds__(NW * 32) dd_kernel(const BwdParams p) {
+  constexpr int NT = NW * 32;
+  constexpr int U = dd_batch(DPL);
   extern __shared__ int32_t bsm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nd = p.nd, ne = p.nQ * p.nq;
   // 16-bit storage: tokens < 65535, entries and positions < 65536
   int32_t* rowptr = bsm;                                                   // [nd + 1]
   float* dsv = reinterpret_cast<float*>(rowptr + nd + 1);                  // [nQ]
-  int32_t* wsum = reinterpret_cast<int32_t*>(dsv + p.nQ);                  // [kBwdWarps] scan scratch
-  uint16_t* counts = reinterpret_cast<uint16_t*>(wsum + kBwdWarps);        // [kBwdWarps][nd] -> offsets
-  uint16_t* list = counts + kBwdWarps * nd;                                // [ne] sorted entry ids
+  int32_t* wsum = reinterpret_cast<int32_t*>(dsv + p.nQ);                  // [NW] scan scratch
+  uint16_t* counts = reinterpret_cast<uint16_t*>(wsum + NW);               // [NW][nd] -> offsets
+  uint16_t* list = counts + NW * nd;                                       // [ne] sorted entry ids
   uint16_t* keys = list + ne;                                              // [ne] token + 1 (0 = skip)
-  const int chunk = (ne + kBwdWarps - 1) / kBwdWarps;
+  const int chunk = (ne + NW - 1) / NW;
   const int e_lo = warp * chunk, e_hi = min(ne, e_lo + chunk);
-  const T* Qp = static_cast<const T*>(p.Q);
+  const uint8_t* Qb = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(lane) * DPL * 2;
+  const size_t qrow_bytes = static_cast<size_t>(p.d) * 2;
 
   for (int64_t b = blockIdx.x; b < p.B; b += gridDim.x) {
     int L = doc_length(p, b);
@@ -114,14 +152,14 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
       if (tid == 0) atomicOr(p.status, kDevErrBadInput);
       L = 0;
     }
-    for (int x = tid; x < kBwdWarps * nd; x += kBwdThreads) counts[x] = 0;
-    for (int q = tid; q < p.nQ; q += kBwdThreads) dsv[q] = __ldg(p.dS + static_cast<int64_t>(q) * p.B + b);
+    for (int x = tid; x < NW * nd; x += NT) counts[x] = 0;
+    for (int q = tid; q < p.nQ; q += NT) dsv[q] = __ldg(p.dS + static_cast<int64_t>(q) * p.B + b);
     // stage the document's argmax entries (coalesced per query row), validated:
     // -1 is only valid for an empty document; anything outside [0, L) is skipped
     bool bad = false;
 #pragma unroll 8
-    for (int e = tid; e < ne; e += kBwdThreads) {
-      const int q = e / p.nq, i = e - q * p.nq;
+    for (int e = tid; e < ne; e += NT) {
+      const int q = p.nq_shift >= 0 ? (e >> p.nq_shift) : e / p.nq, i = e - q * p.nq;
       int key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
       if (key < 0 || key >= L) {
         if (!(key == -1 && L == 0)) bad = true;
@@ -143,11 +181,11 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
     __syncthreads();
     // scan over (key, warp): offsets[w][j] = start[j] + sum_{w' < w} counts[w'][j]
     {
-      const int per = (nd + kBwdThreads - 1) / kBwdThreads;
+      const int per = (nd + NT - 1) / NT;
       const int j0 = tid * per, j1 = min(nd, j0 + per);
       int run = 0;
       for (int j = j0; j < j1; ++j)
-        for (int w = 0; w < kBwdWarps; ++w) run += counts[w * nd + j];
+        for (int w = 0; w < NW; ++w) run += counts[w * nd + j];
       // block-wide exclusive scan of the per-thread totals
       int incl = run;
 #pragma unroll
@@ -162,7 +200,7 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
       base += incl - run;
       for (int j = j0; j < j1; ++j) {
         rowptr[j] = base;
-        for (int w = 0; w < kBwdWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
           const int c = counts[w * nd + j];
           counts[w * nd + j] = static_cast<uint16_t>(base);
           base += c;
@@ -186,41 +224,46 @@ __global__ void __launch_bounds__(kBwdThreads) dd_kernel(const BwdParams p) {
       __syncwarp();
     }
     __syncthreads();
-    // destination-owned rows: warp per row j of dD[b]
-    for (int j = warp; j < nd; j += kBwdWarps) {
+    // destination-owned rows: warp per row j of dD[b]. Up to U entries' Q rows
+    // are loaded together (their FMAs then run in list order, which is
+    // ascending entry order: the sum does not depend on scheduling).
+    for (int j = warp; j < nd; j += NW) {
       float acc[DPL];
 #pragma unroll
       for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
       const int r0 = rowptr[j], r1 = rowptr[j + 1];
-      // gathers of up to 4 entries are issued together; the FMAs stay in entry order
-      for (int r = r0; r < r1; r += 4) {
-        float2 x[4][DPL / 2];
-        float gq[4];
+      for (int r = r0; r < r1; r += U) {
+        uint32_t x[U][DPL / 2];
+        float gq[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
           gq[u] = 0.f;
           if (r + u < r1) {
             const int e = list[r + u];
             gq[u] = dsv[p.nq_shift >= 0 ? (e >> p.nq_shift) : (e / p.nq)];
-            const T* qrow = Qp + static_cast<int64_t>(e) * p.d;   // Q[q, i, :] with e = q*nq + i
-#pragma unroll
-            for (int k = 0; k < DPL; k += 2) x[u][k / 2] = load2<T>(qrow + k * 32 + 2 * lane);
+            load_row_words<DPL>(Qb + static_cast<size_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :] with e = q*nq + i
           }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < U; ++u)
           if (r + u < r1) {
 #pragma unroll
-            for (int k = 0; k < DPL; k += 2) {
-              acc[k] = fmaf(gq[u], x[u][k / 2].x, acc[k]);
-              acc[k + 1] = fmaf(gq[u], x[u][k / 2].y, acc[k + 1]);
+            for (int k = 0; k < DPL / 2; ++k) {
+              const float2 f = unpack2<T>(x[u][k]);
+              acc[2 * k] = fmaf(gq[u], f.x, acc[2 * k]);
+              acc[2 * k + 1] = fmaf(gq[u], f.y, acc[2 * k + 1]);
             }
           }
       }
-      float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d);
+      float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DPL;
+      if constexpr (DPL % 4 == 0) {
 #pragma unroll
-      for (int k = 0; k < DPL; k += 2)
-        *reinterpret_cast<float2*>(drow + k * 32 + 2 * lane) = make_float2(acc[k], acc[k + 1]);
+        for (int k = 0; k < DPL; k += 4)
+          __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < DPL; k += 2) __stcs(reinterpret_cast<float2*>(drow + k), make_float2(acc[k], acc[k + 1]));
+      }
     }
     __syncthreads();
   }
@@ -257,7 +300,12 @@ __global__ void __launch_bounds__(kDqThreads, 2) dq_kernel(const BwdParams p) {
   const bool active = rr < R && i < p.nq;  // d / 32 need not divide the thread count
   const int64_t bs = (p.B * blockIdx.y) / p.splits, be = (p.B * (blockIdx.y + 1)) / p.splits;
   const int64_t n = be - bs;
-  const T* Dp = static_cast<const T*>(p.D) + part * 32;
+  // The row is cut into 4 bands of d / 4 elements; the row's tpr threads take
+  // 8 consecutive elements of each band, so the threads of a row copy a band's
+  // bytes contiguously and every 16-byte copy instruction of a warp covers
+  // whole 32-byte sectors. acc[8 v + h] is element v * band + 8 part + h.
+  const int band = d / 4;
+  const T* Dp = static_cast<const T*>(p.D) + part * 8;
   const int32_t* arow = p.argmax + static_cast<int64_t>(q) * p.B * p.nq + i;
   const float* grow = p.dS + static_cast<int64_t>(q) * p.B;
   const uint32_t slot0 = smem_u32(dq_raw) + static_cast<uint32_t>(tid) * 16;
@@ -289,7 +337,7 @@ __global__ void __launch_bounds__(kDqThreads, 2) dq_kernel(const BwdParams p) {
     const uint32_t dst = slot0 + static_cast<uint32_t>(slot * 4 * kDqThreads * 16);
     const T* src = a >= 0 ? Dp + ((bs + j) * p.nd + a) * static_cast<int64_t>(d) : Dp;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) cp_async16(dst + v * kDqThreads * 16, src + v * 8, a >= 0 ? 16u : 0u);
+    for (int v = 0; v < 4; ++v) cp_async16(dst + v * kDqThreads * 16, src + v * band, a >= 0 ? 16u : 0u);
   };
 
 #pragma unroll
@@ -334,9 +382,13 @@ __global__ void __launch_bounds__(kDqThreads, 2) dq_kernel(const BwdParams p) {
   cp_async_wait<0>();
   if (active) {
     float* out = (p.splits > 1 ? p.partial + static_cast<int64_t>(blockIdx.y) * p.nQ * p.nq * d : p.dQ) +
-                 (static_cast<int64_t>(q) * p.nq + i) * d + part * 32;
+                 (static_cast<int64_t>(q) * p.nq + i) * d + part * 8;
 #pragma unroll
-    for (int k = 0; k < 32; k += 4) *reinterpret_cast<float4*>(out + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
+    for (int v = 0; v < 4; ++v)
+#pragma unroll
+      for (int h = 0; h < 8; h += 4)
+        *reinterpret_cast<float4*>(out + v * band + h) =
+            make_float4(acc[8 * v + h], acc[8 * v + h + 1], acc[8 * v + h + 2], acc[8 * v + h + 3]);
   }
   if (bad) atomicOr(p.status, kDevErrBadInput);
 }
@@ -360,19 +412,15 @@ __global__ void dq_reduce_kernel(const BwdParams p) {
   }
 }
 
-template <typename T>
-maxsim_status launch_dd(const BwdParams& p, const DeviceInfo* dev, cudaStream_t stream) {
-  const size_t smem = (static_cast<size_t>(p.nd) + 1 + p.nQ + kBwdWarps) * 4 +
-                      (static_cast<size_t>(kBwdWarps) * p.nd + 2 * static_cast<size_t>(p.nQ) * p.nq) * 2;
-  if (smem > static_cast<size_t>(dev->max_smem_optin)) return MAXSIM_ERR_UNSUPPORTED;
-  const int64_t want = static_cast<int64_t>(dev->sm_count) * 2;
-  const int grid = static_cast<int>(p.B < want ? p.B : want);
+template <typename T, int NW>
+maxsim_status launch_dd_nw(const BwdParams& p, size_t smem, int grid, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   switch (p.d / 32) {
-#define MSIM_DD(DPL)                                                                                           \
-  case DPL:                                                                                                    \
-    e = cudaFuncSetAttribute(dd_kernel<T, DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-    if (e == cudaSuccess) dd_kernel<T, DPL><<<grid, kBwdThreads, smem, stream>>>(p);                           \
+#define MSIM_DD(DPL)                                                                                        \
+  case DPL:                                                                                                 \
+    e = cudaFuncSetAttribute(dd_kernel<T, DPL, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,           \
+                             static_cast<int>(smem));                                                       \
+    if (e == cudaSuccess) dd_kernel<T, DPL, NW><<<grid, NW * 32, smem, stream>>>(p);                        \
     break;
     MSIM_DD(2) MSIM_DD(4) MSIM_DD(6) MSIM_DD(8) MSIM_DD(10) MSIM_DD(12) MSIM_DD(14) MSIM_DD(16)
     MSIM_DD(18) MSIM_DD(20) MSIM_DD(22) MSIM_DD(24) MSIM_DD(26) MSIM_DD(28) MSIM_DD(30) MSIM_DD(32)
@@ -381,6 +429,20 @@ maxsim_status launch_dd(const BwdParams& p, const DeviceInfo* dev, cudaStream_t 
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
   return MAXSIM_OK;
+}
+
+// dD: 16 warps per CTA and two CTAs per SM when the per-document sort fits
+// twice in shared memory (the ColPali shape: 100 KB), else 8 warps.
+template <typename T>
+maxsim_status launch_dd(const BwdParams& p, const DeviceInfo* dev, cudaStream_t stream) {
+  const int ne = p.nQ * p.nq;
+  const size_t budget = static_cast<size_t>(dev->max_smem_optin);
+  const size_t smem16 = dd_smem_bytes(16, p.nd, p.nQ, ne), smem8 = dd_smem_bytes(8, p.nd, p.nQ, ne);
+  const int64_t want = static_cast<int64_t>(dev->sm_count) * 2;
+  const int grid = static_cast<int>(p.B < want ? p.B : want);
+  if (2 * smem16 + 2048 <= budget + 1024) return launch_dd_nw<T, 16>(p, smem16, grid, stream);
+  if (smem8 > budget) return MAXSIM_ERR_UNSUPPORTED;
+  return launch_dd_nw<T, 8>(p, smem8, grid, stream);
 }
 
 template <typename T>

@@ -66,6 +66,7 @@ constexpr int kMaxAcc = 4;
 constexpr int kMaxFin = 5;           // documents finished per tile (4 slots + pass end)
 
 struct FwdTcParams {
+  const int32_t* order;     // walk position -> document index, or null (identity)
   const int32_t* doc_len;   // padded layout, may be null
   const int64_t* offsets;   // CSR layout
   int64_t B;
@@ -162,10 +163,24 @@ struct Bars {
   }
 };
 
-// Rows of document b (start row and length); out-of-range descriptions are
-// reported as bad and scored as empty documents.
-__device__ __forceinline__ int64_t doc_rows(const FwdTcParams& p, int64_t b, int64_t& start, bool& bad) {
+// Document scored at walk position `pos`: the identity, or order[pos] when a
+// document order is given (-1 if that entry is outside [0, B)).
+__device__ __forceinline__ int64_t doc_at(const FwdTcParams& p, int64_t pos) {
+  if (!p.order) return pos;
+  const int64_t b = __ldg(p.order + pos);
+  return (b < 0 || b >= p.B) ? -1 : b;
+}
+
+// Rows of the document at walk position `pos` (start row and length);
+// out-of-range descriptions are reported as bad and scored as empty documents.
+__device__ __forceinline__ int64_t doc_rows(const FwdTcParams& p, int64_t pos, int64_t& start, bool& bad) {
   bad = false;
+  const int64_t b = doc_at(p, pos);
+  if (b < 0) {
+    bad = true;
+    start = 0;
+    return 0;
+  }
   if (p.csr) {
     const int64_t s = __ldg(p.offsets + b), e = __ldg(p.offsets + b + 1);
     if (s < 0 || e < s || e > p.total_rows) {
@@ -273,6 +288,10 @@ template <int NC>
 __device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& br, const CUtensorMap* tm_d128,
                              const CUtensorMap* tm_d32, const CUtensorMap* tm_q, int64_t b0, int64_t b1) {
   const int lane = threadIdx.x & 31;
+  // Test-only fault switch (maxsim_debug_set_faults): the loader issues
+  // nothing, so every other role's bounded wait runs out and the CTA aborts
+  // with no copy or MMA in flight.
+  if (debug_faults(p.status) & kDebugStallFwdLoader) return;
   const int S = p.stages, KB = p.KB, NQS = p.n_qslots;
   const uint32_t qbytes = static_cast<uint32_t>(KB) * NC * 128;
   const uint64_t policy = l2_policy_evict_first();
@@ -582,7 +601,7 @@ __device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) 
       const int qc = c * NC + g * 32 + lane;
       if (qc < p.nq) {
         sum += rm[g];
-        if (ARGMAX) p.argmax[(static_cast<int64_t>(q) * p.B + doc) * p.nq + qc] = ra[g];
+        if (ARGMAX && doc >= 0) p.argmax[(static_cast<int64_t>(q) * p.B + doc) * p.nq + qc] = ra[g];
       }
     }
     return sum;
@@ -601,8 +620,8 @@ __device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) 
         const bool last_chunk = c == p.n_chunks - 1;
         // empty documents of the group: score 0, argmax -1 (no slots, no MMA)
         for (int dl = lane; dl < n_docs; dl += 32) {
-          if (T->doc_len[dl] == 0) {
-            const int64_t b = first + dl;
+          const int64_t b = doc_at(p, first + dl);
+          if (T->doc_len[dl] == 0 && b >= 0) {
             if (ARGMAX)
               for (int col = 0; col < NC; ++col) {
                 const int qc = c * NC + col;
@@ -624,7 +643,7 @@ __device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) 
           for (int w = 0; w < nslot; ++w) {
             const int64_t dg = first + T->slot_doc[i0 + w];
             if (dg != cur) {
-              if (cur >= 0) fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, cur, q));
+              if (cur >= 0) fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, doc_at(p, cur), q));
               cur = dg;
 #pragma unroll
               for (int g = 0; g < NG; ++g) {
@@ -653,7 +672,7 @@ __device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) 
             pph ^= 1u;
           }
           if (p.multipass && t == n_tiles - 1 && cur >= 0) {
-            fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, cur, q));
+            fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, doc_at(p, cur), q));
             cur = -1;
           }
           if (nfin > 0) {
@@ -672,13 +691,15 @@ __device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) 
                   total = fin_sum[f];
                   b = fin_doc[f];
                 }
-              const int64_t o = static_cast<int64_t>(q) * p.B + b;
+              const int64_t bd = doc_at(p, b);       // b is a walk position
+              const int64_t o = static_cast<int64_t>(q) * p.B + bd;
               if (p.n_chunks == 1) {
-                p.out[o] = total;
+                if (bd >= 0) p.out[o] = total;
               } else {
                 const int dl = static_cast<int>(b - first);
                 const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
-                if (last_chunk) p.out[o] = g2; else sm.gsum[dl] = g2;
+                if (!last_chunk) sm.gsum[dl] = g2;
+                else if (bd >= 0) p.out[o] = g2;
               }
             }
           }
@@ -690,10 +711,11 @@ __device__ void run_merge(const FwdTcParams& p, const Smem& sm, const Bars& br) 
   }
   // end of work: the last document of a single-pass walk is still open
   if (!p.multipass && cur >= 0) {
-    float sum = doc_sum(0, cur, 0);
+    const int64_t bd = doc_at(p, cur);
+    float sum = doc_sum(0, bd, 0);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) p.out[cur] = sum;
+    if (lane == 0 && bd >= 0) p.out[bd] = sum;
   }
 }
 
@@ -775,16 +797,18 @@ cudaError_t launch_variant(const CUtensorMap& d128, const CUtensorMap& d32, cons
 
 maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const void* D, int64_t total_rows,
                             int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
-                            int is_bf16, float* out, int32_t* argmax, cudaStream_t stream) {
+                            int is_bf16, float* out, int32_t* argmax, cudaStream_t stream, const int32_t* order) {
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
   if (d % 64 != 0 || d < 64 || d > 1024) return MAXSIM_ERR_UNSUPPORTED;
   // rows are int32 TMA coordinates and chunk indices are packed above 6 bits
   if (total_rows < 1 || total_rows > (static_cast<int64_t>(1) << 30)) return MAXSIM_ERR_UNSUPPORTED;
   // long queries: query-major kernel (document tiles reused across 512 query rows)
-  if (fwd_qm_applicable(nq, d, total_rows))
+  if (fwd_qm_applicable(nq, d, total_rows)) {
+    if (order) return MAXSIM_ERR_UNSUPPORTED;   // the long-query kernel walks documents in index order
     return launch_fwd_qm(Q, n_queries, nq, d, D, total_rows, csr, doc_len, offsets, B, nd, is_bf16, out, argmax,
                          stream);
+  }
   const int KB = d / 64;
 
   // Query chunk width NC = 32 * NG: as wide as nq needs (up to 256 columns,
@@ -828,6 +852,7 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
     return MAXSIM_ERR_CUDA;
 
   FwdTcParams p;
+  p.order = order;
   p.doc_len = doc_len;
   p.offsets = offsets;
   p.B = B;

@@ -23,9 +23,19 @@ const DeviceInfo* device_info();
 // Forward scoring on tcgen05 tensor cores (bf16 / fp16 inputs).
 // Documents are given either padded (csr = 0: rows b*nd .. b*nd+L_b-1, L_b
 // from doc_len or nd) or CSR (csr = 1: rows offsets[b] .. offsets[b+1]-1).
+// `order` (a permutation of [0, B), or null) is the order in which documents
+// are walked; outputs always land at the documents' own indices. Not
+// supported by the long-query kernel (MAXSIM_ERR_UNSUPPORTED).
 maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const void* D, int64_t total_rows,
                             int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
-                            int is_bf16, float* out, int32_t* argmax, cudaStream_t stream);
+                            int is_bf16, float* out, int32_t* argmax, cudaStream_t stream,
+                            const int32_t* order = nullptr);
+
+// Length-bucketed document order: a stable counting sort of documents by
+// their number of 8-row granules ceil(L_b / 8), ascending, into order[B].
+size_t length_order_workspace_bytes(int64_t B, int nd);
+maxsim_status launch_length_order(const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
+                                  int32_t* order, void* workspace, cudaStream_t stream);
 
 // Query-major forward for long queries (a few hundred to 1024 tokens); same
 // arguments and outputs as launch_fwd_tc, which calls it when applicable.

@@ -3,7 +3,8 @@
 // allocation, UMMA issue/commit, TMEM loads) and bounded waits.
 //
 // Every wait in this library is bounded: it polls a CTA-wide abort flag and
-// the global nanosecond timer, and after kWaitTimeoutNs it records
+// the global nanosecond timer, and after its bound (kWaitTimeoutNs unless a
+// test set another in the status block) it records
 // MAXSIM_DEVERR_TIMEOUT in the caller's status word, raises the abort flag
 // and returns false so the kernel can drain and exit.
 #pragma once
@@ -17,6 +18,19 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 constexpr uint32_t kFastSpins = 1024;
 constexpr unsigned kDevErrTimeout = 0x1u;
 constexpr unsigned kDevErrBadInput = 0x2u;
+constexpr unsigned kDebugStallFwdLoader = 0x1u;
+
+// `status` points at the device's status block: word 0 the status bits, word
+// 1 test-only fault switches, words 2-3 the wait bound in ns (0 = default).
+// The bound is read once a wait has left its fast polling path. Drains after
+// an abort always use the default bound.
+__device__ __forceinline__ uint64_t wait_limit_ns(const unsigned* status) {
+  const uint64_t v = *reinterpret_cast<const volatile unsigned long long*>(status + 2);
+  return v ? v : kWaitTimeoutNs;
+}
+__device__ __forceinline__ unsigned debug_faults(const unsigned* status) {
+  return *reinterpret_cast<const volatile unsigned*>(status + 1);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -85,12 +99,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   // so it never sits on the critical path of a normal hand-off.
   for (uint32_t it = 0; it < kFastSpins; ++it)
     if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns(), lim = wait_limit_ns(status);
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > lim) {
         atomicOr(status, kDevErrTimeout);
         *abort_flag = 1;
         return false;
@@ -101,12 +115,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 static __device__ __noinline__ bool mbar_wait_slow_a(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned* status) {
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns(), lim = wait_limit_ns(status);
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_a(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > lim) {
         atomicOr(status, kDevErrTimeout);
         *abort_flag = 1;
         return false;
@@ -138,12 +152,12 @@ __device__ __forceinline__ bool mbar_test_wait_a(uint32_t bar, uint32_t parity) 
 }
 static __device__ __noinline__ bool mbar_poll_slow_a(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                      unsigned* status) {
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns(), lim = wait_limit_ns(status);
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_wait_a(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > lim) {
         atomicOr(status, kDevErrTimeout);
         *abort_flag = 1;
         return false;
@@ -170,13 +184,13 @@ __device__ __forceinline__ bool mbar_wait_inl_a(uint32_t bar, uint32_t parity, v
 #pragma unroll 1
   for (uint32_t it = 0; it < kFastSpins; ++it)
     if (mbar_try_wait_a(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns(), lim = wait_limit_ns(status);
 #pragma unroll 1
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_a(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > lim) {
         atomicOr(status, kDevErrTimeout);
         *abort_flag = 1;
         return false;
@@ -189,13 +203,13 @@ __device__ __forceinline__ bool mbar_poll_inl_a(uint32_t bar, uint32_t parity, v
 #pragma unroll 1
   for (uint32_t it = 0; it < 4 * kFastSpins; ++it)
     if (mbar_test_wait_a(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns(), lim = wait_limit_ns(status);
 #pragma unroll 1
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_wait_a(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > lim) {
         atomicOr(status, kDevErrTimeout);
         *abort_flag = 1;
         return false;

@@ -106,3 +106,21 @@ def test_backward_halves_validate_before_launch(lib):
     assert lib.maxsim_backward_dq(1, 32, 128, fake, 10, 64, None, 0, fake, fake, None, None, 0, None) == 1
     assert m.maxsim_backward_workspace_size(1, 32, 128, 5000, 64) > 0
     assert lib.maxsim_backward_dq(1, 32, 128, fake, 5000, 64, None, 0, fake, fake, fake, None, 0, None) == 5
+
+
+def test_debug_fault_switch_validates_flags(lib):
+    """The test-only fault switch rejects unknown bits before touching a device."""
+    assert lib.maxsim_debug_set_faults(0x80, 0) == 1
+
+
+def test_length_order_validates_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # both layouts at once / missing workspace / missing output
+    assert lib.maxsim_length_order(fake, fake, 10, 64, fake, fake, 1 << 20, None) == 1
+    assert lib.maxsim_length_order(fake, None, 10, 64, fake, None, 0, None) == 5
+    assert lib.maxsim_length_order(fake, None, 10, 64, None, fake, 1 << 20, None) == 1
+    assert m.maxsim_length_order_workspace_size(10, 64, 0) > 0
+    # ordered scoring: fp32 unsupported, missing order rejected
+    assert lib.maxsim_score_ordered(fake, 1, 32, 128, fake, 10, 128, None, fake, 2, fake, None, None) == 2
+    assert lib.maxsim_score_ordered(fake, 1, 32, 128, fake, 10, 128, None, None, 0, fake, None, None) == 1
