@@ -55,15 +55,17 @@ __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
                      __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
 }
 
-template <typename T>
-__device__ __forceinline__ float2 load2(const T* p);
-template <>
-__device__ __forceinline__ float2 load2<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-}
-template <>
-__device__ __forceinline__ float2 load2<__half>(const __half* p) {
-  return __half22float2(*reinterpret_cast<const __half2*>(p));
+// (a0, a1) += g * (x0, x1) as one packed fp32x2 FMA: two IEEE round-to-nearest
+// FMAs, bit-identical to two fmaf calls, in one issue slot.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float g, float2 x) {
+  asm("{\n\t.reg .b64 acc, xv, gv;\n\t"
+      "mov.b64 acc, {%0, %1};\n\t"
+      "mov.b64 xv, {%2, %3};\n\t"
+      "mov.b64 gv, {%4, %4};\n\t"
+      "fma.rn.f32x2 acc, gv, xv, acc;\n\t"
+      "mov.b64 {%0, %1}, acc;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x.x), "f"(x.y), "f"(g));
 }
 
 struct BwdParams {
@@ -76,11 +78,19 @@ struct BwdParams {
   float* dD;
   int64_t B;
   int nQ, nq, d, nd;
-  int nq_shift;      // log2(nq) when nq is a power of two, else -1
+  uint32_t nq_inv;   // ceil(2^32 / nq) for nq > 1 (0 for nq = 1): e / nq = umulhi(e, nq_inv) for e < 2^16
   int splits;        // dQ document ranges (partials summed in range order)
   float* partial;    // [splits][nQ][nq][d] workspace (splits > 1)
   unsigned* status;
 };
+
+// Query of argmax entry e = q * nq + i (e < 2^16): a multiply-high by the
+// rounded-up reciprocal, exact here because with nq_inv * nq = 2^32 + eps
+// (0 <= eps < nq) the excess e * eps / 2^32 stays below 1 (e, eps < 2^16).
+__device__ __forceinline__ int entry_query(const BwdParams& p, int e) {
+  const int q = static_cast<int>(__umulhi(static_cast<uint32_t>(e), p.nq_inv));
+  return p.nq_inv ? q : e;   // nq = 1: the entry is the query
+}
 
 __device__ __forceinline__ int doc_length(const BwdParams& p, int64_t b) {
   if (!p.doc_len) return p.nd;
@@ -120,15 +130,16 @@ __device__ __forceinline__ void load_row_words(const void* src, uint32_t (&w)[DP
 }
 
 // Entries of one destination row gathered per batch: enough Q-row loads in
-// flight per lane to cover L2 latency, within the register budget.
-__host__ __device__ constexpr int dd_batch(int dpl) { return dpl <= 4 ? 8 : dpl <= 8 ? 4 : 2; }
+// flight per lane to cover L2 latency, within the register budget of two
+// 16-warp CTAs per SM (64 registers a thread).
+__host__ __device__ constexpr int dd_batch(int dpl) { return dpl <= 4 ? 8 : dpl <= 8 ? 4 : dpl <= 16 ? 2 : 1; }
 
 __host__ __device__ constexpr size_t dd_smem_bytes(int nw, int nd, int nQ, int ne) {
   return (static_cast<size_t>(nd) + 1 + nQ + nw) * 4 + (static_cast<size_t>(nw) * nd + 2 * static_cast<size_t>(ne)) * 2;
 }
 
 template <typename T, int DPL, int NW>
-__global__ void __launch_bounds__(NW * 32) dd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(NW * 32, 2) dd_kernel(const BwdParams p) {
   constexpr int NT = NW * 32;
   constexpr int U = dd_batch(DPL);
   extern __shared__ int32_t bsm[];
@@ -144,7 +155,7 @@ __global__ void __launch_bounds__(NW * 32) dd_kernel(const BwdParams p) {
   const int chunk = (ne + NW - 1) / NW;
   const int e_lo = warp * chunk, e_hi = min(ne, e_lo + chunk);
   const uint8_t* Qb = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(lane) * DPL * 2;
-  const size_t qrow_bytes = static_cast<size_t>(p.d) * 2;
+  const uint32_t qrow_bytes = static_cast<uint32_t>(p.d) * 2;   // e * qrow_bytes < 2^16 * 2^11
 
   for (int64_t b = blockIdx.x; b < p.B; b += gridDim.x) {
     int L = doc_length(p, b);
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(NW * 32) dd_kernel(const BwdParams p) {
     bool bad = false;
 #pragma unroll 8
     for (int e = tid; e < ne; e += NT) {
-      const int q = p.nq_shift >= 0 ? (e >> p.nq_shift) : e / p.nq, i = e - q * p.nq;
+      const int q = entry_query(p, e), i = e - q * p.nq;
       int key = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b) * p.nq + i);
       if (key < 0 || key >= L) {
         if (!(key == -1 && L == 0)) bad = true;
@@ -232,28 +243,22 @@ __global__ void __launch_bounds__(NW * 32) dd_kernel(const BwdParams p) {
 #pragma unroll
       for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
       const int r0 = rowptr[j], r1 = rowptr[j + 1];
+      // Branch-free batches: a batch running past the row's last entry repeats
+      // that entry with weight 0 (its Q row is one this row adds anyway).
       for (int r = r0; r < r1; r += U) {
         uint32_t x[U][DPL / 2];
         float gq[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          gq[u] = 0.f;
-          if (r + u < r1) {
-            const int e = list[r + u];
-            gq[u] = dsv[p.nq_shift >= 0 ? (e >> p.nq_shift) : (e / p.nq)];
-            load_row_words<DPL>(Qb + static_cast<size_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :] with e = q*nq + i
-          }
+          const int e = list[min(r + u, r1 - 1)];
+          const float g = dsv[entry_query(p, e)];
+          gq[u] = r + u < r1 ? g : 0.f;
+          load_row_words<DPL>(Qb + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :] with e = q*nq + i
         }
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (r + u < r1) {
 #pragma unroll
-            for (int k = 0; k < DPL / 2; ++k) {
-              const float2 f = unpack2<T>(x[u][k]);
-              acc[2 * k] = fmaf(gq[u], f.x, acc[2 * k]);
-              acc[2 * k + 1] = fmaf(gq[u], f.y, acc[2 * k + 1]);
-            }
-          }
+          for (int k = 0; k < DPL / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
       }
       float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DPL;
       if constexpr (DPL % 4 == 0) {
@@ -271,32 +276,38 @@ __global__ void __launch_bounds__(NW * 32) dd_kernel(const BwdParams p) {
 
 // ------------------------------------------------------------------- dQ
 // Each thread owns 32 dimensions of one destination row, so a CTA holds
-// 256 / (d / 32) rows. Per document a thread copies its 64-byte slice of the
-// selected D row into its own shared-memory slot with 16-byte cp.async
-// (zero-fill for a skipped entry), kDqDepth documents ahead of the one it
-// accumulates; the argmax entries and dS values are fetched into registers
-// 2 * kDqDepth - 1 documents ahead, so neither dependent load stalls the
-// accumulation. No data is shared between threads, so the pipeline needs
-// no barrier. blockIdx.y picks one of `splits` contiguous document ranges;
-// with one range the sum goes straight to dQ, otherwise to partial[range]
-// for dq_reduce_kernel.
+// R = 256 / (d / 32) rows of one query. Documents are taken in blocks of
+// K = 2048 / R: the block's argmax entries for the CTA's rows (K x R
+// int32, contiguous per document), its dS values and document lengths are
+// loaded into registers one block ahead (eight entries per thread) and
+// staged in shared memory, so reading them never waits on memory. Per
+// document a thread copies its 64-byte slice of the selected D row into its
+// own shared-memory slot with 16-byte cp.async (zero-fill for a skipped
+// entry), kDqDepth documents ahead of the one it accumulates. blockIdx.y
+// picks one of `splits` contiguous document ranges; with one range the sum
+// goes straight to dQ, otherwise to partial[range] for dq_reduce_kernel.
 constexpr int kDqThreads = 256;
 constexpr int kDqDepth = 6;                 // documents in flight per thread
-constexpr int kDqRing = 2 * kDqDepth;       // argmax / dS register ring
+constexpr int kDqStage = 2048;              // argmax entries staged per block (8 per thread)
 
 __host__ __device__ constexpr int dq_rows(int d) { return kDqThreads / (d / 32); }
-// [depth][4 x 16 B][thread]: the v-th 16 bytes of all threads are contiguous
-__host__ __device__ constexpr size_t dq_smem_bytes() { return static_cast<size_t>(kDqDepth) * 4 * kDqThreads * 16; }
+__host__ __device__ constexpr int dq_block_docs(int d) { return kDqStage / dq_rows(d); }
+// [depth][4 x 16 B][thread] row slices (the v-th 16 bytes of all threads
+// contiguous), then [2][kDqStage] argmax entries, [2][K] dS and [2][K] lengths
+__host__ __device__ constexpr size_t dq_smem_bytes(int d) {
+  return static_cast<size_t>(kDqDepth) * 4 * kDqThreads * 16 + 2 * kDqStage * 4 + 2 * 2 * dq_block_docs(d) * 4;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kDqThreads, 2) dq_kernel(const BwdParams p) {
   extern __shared__ __align__(16) uint8_t dq_raw[];
   const int tid = threadIdx.x;
-  const int d = p.d, tpr = d / 32, R = dq_rows(d);
+  const int d = p.d, tpr = d / 32, R = dq_rows(d), K = dq_block_docs(d);
   const int blocks_per_q = (p.nq + R - 1) / R;
   const int q = blockIdx.x / blocks_per_q;
+  const int i0 = (blockIdx.x - q * blocks_per_q) * R;
   const int rr = tid / tpr, part = tid - rr * tpr;
-  const int i = (blockIdx.x - q * blocks_per_q) * R + rr;
+  const int i = i0 + rr;
   const bool active = rr < R && i < p.nq;  // d / 32 need not divide the thread count
   const int64_t bs = (p.B * blockIdx.y) / p.splits, be = (p.B * (blockIdx.y + 1)) / p.splits;
   const int64_t n = be - bs;
@@ -306,76 +317,109 @@ __global__ void __launch_bounds__(kDqThreads, 2) dq_kernel(const BwdParams p) {
   // whole 32-byte sectors. acc[8 v + h] is element v * band + 8 part + h.
   const int band = d / 4;
   const T* Dp = static_cast<const T*>(p.D) + part * 8;
-  const int32_t* arow = p.argmax + static_cast<int64_t>(q) * p.B * p.nq + i;
-  const float* grow = p.dS + static_cast<int64_t>(q) * p.B;
   const uint32_t slot0 = smem_u32(dq_raw) + static_cast<uint32_t>(tid) * 16;
+  int32_t* am_s = reinterpret_cast<int32_t*>(dq_raw + static_cast<size_t>(kDqDepth) * 4 * kDqThreads * 16);  // [2][K][R]
+  float* ds_s = reinterpret_cast<float*>(am_s + 2 * kDqStage);                                               // [2][K]
+  int32_t* len_s = reinterpret_cast<int32_t*>(ds_s + 2 * K);                                                 // [2][K]
   bool bad = false;
 
-  // entry j (document bs + j): argmax a, dS g; a = -1 marks "nothing to add"
-  int ra[kDqRing];
-  float rg[kDqRing];
-  auto fetch = [&](int64_t j, int& a, float& g) {
-    a = -1;
-    g = 0.f;
-    if (active && j < n) {
-      const int64_t b = bs + j;
-      const int v = __ldg(arow + b * p.nq);
-      const int L = doc_length(p, b);  // -1: the document's length itself is invalid
-      if (v >= 0) {
-        if (v < L) {
-          a = v;
-          g = __ldg(grow + b);
-        } else {
-          bad = true;
-        }
-      } else if (v < -1) {
-        bad = true;
-      }
+  // block staging: entry x = tid + 256 m is document x / R, row x % R of the block
+  int sa[kDqStage / kDqThreads];
+  float sg = 0.f;
+  int sl = 0;
+  auto load_block = [&](int64_t blk) {
+    const int64_t b0 = bs + blk * K;
+#pragma unroll
+    for (int m = 0; m < kDqStage / kDqThreads; ++m) {
+      const int x = tid + kDqThreads * m, kk = x / R, r = x - kk * R;
+      sa[m] = -1;
+      if (blk * K + kk < n && i0 + r < p.nq)
+        sa[m] = __ldg(p.argmax + (static_cast<int64_t>(q) * p.B + b0 + kk) * p.nq + i0 + r);
+    }
+    if (tid < K && blk * K + tid < n) {
+      sg = __ldg(p.dS + static_cast<int64_t>(q) * p.B + b0 + tid);
+      sl = doc_length(p, b0 + tid);   // -1: the document's length itself is invalid
     }
   };
-  auto issue = [&](int64_t j, int a, int slot) {
-    const uint32_t dst = slot0 + static_cast<uint32_t>(slot * 4 * kDqThreads * 16);
-    const T* src = a >= 0 ? Dp + ((bs + j) * p.nd + a) * static_cast<int64_t>(d) : Dp;
+  auto store_block = [&](int buf) {
 #pragma unroll
-    for (int v = 0; v < 4; ++v) cp_async16(dst + v * kDqThreads * 16, src + v * band, a >= 0 ? 16u : 0u);
+    for (int m = 0; m < kDqStage / kDqThreads; ++m) am_s[buf * kDqStage + tid + kDqThreads * m] = sa[m];
+    if (tid < K) {
+      ds_s[buf * K + tid] = sg;
+      len_s[buf * K + tid] = sl;
+    }
+  };
+  // argmax of entry j for this thread's row (staged at block position kk of
+  // buffer buf), validated against the document's length (-1: nothing to
+  // add; a bad entry also sets the bad-input bit)
+  auto entry = [&](int64_t j, int kk, int buf) -> int {
+    if (!active || j >= n) return -1;
+    const int v = am_s[buf * kDqStage + kk * R + rr];
+    const int L = len_s[buf * K + kk];
+    if (v >= 0 && v < L) return v;
+    if (v < -1 || v >= 0) bad = true;
+    return -1;
   };
 
+  load_block(0);
+  store_block(0);
+  __syncthreads();
+  if (K < n) load_block(1);
+  // issue pointer: entry ij at block position ikk of block iblk (buffer iblk & 1)
+  int64_t ij = 0, iblk = 0;
+  int ikk = 0;
+  const T* dbase = Dp + bs * static_cast<int64_t>(p.nd) * d;   // document bs + ij's rows
+  const int64_t doc_elems = static_cast<int64_t>(p.nd) * d;
+  // The copy of an entry into ring slot `slot`; returns the weight to apply
+  // when it is consumed (0 for nothing to add: the slot is then zero-filled,
+  // so the consumer's FMAs add zeros and need no branch).
+  auto issue_next = [&](int slot) -> float {
+    if (ikk == 0 && iblk > 0 && ij < n) {
+      // entering block iblk: stage it in the buffer block iblk - 2 used (every
+      // thread has consumed that block: the consumer runs kDqDepth - 1 entries
+      // behind, and K > kDqDepth), then start loading block iblk + 1
+      __syncthreads();
+      store_block(static_cast<int>(iblk & 1));
+      __syncthreads();
+      if ((iblk + 1) * K < n) load_block(iblk + 1);
+    }
+    const int buf = static_cast<int>(iblk & 1);
+    const int a = entry(ij, ikk, buf);
+    const float g = a >= 0 ? ds_s[buf * K + ikk] : 0.f;
+    const uint32_t dst = slot0 + static_cast<uint32_t>(slot * 4 * kDqThreads * 16);
+    const T* src = a >= 0 ? dbase + static_cast<uint32_t>(a) * static_cast<uint32_t>(d) : Dp;
 #pragma unroll
-  for (int k = 0; k < kDqRing - 1; ++k) fetch(k, ra[k], rg[k]);
-#pragma unroll
-  for (int k = 0; k < kDqDepth - 1; ++k) {
-    issue(k, ra[k], k);
+    for (int v = 0; v < 4; ++v) cp_async16(dst + v * kDqThreads * 16, src + v * band, a >= 0 ? 16u : 0u);
     cp_async_commit();
-  }
+    ++ij;
+    dbase += doc_elems;
+    if (++ikk == K) {
+      ikk = 0;
+      ++iblk;
+    }
+    return g;
+  };
+  float gw[kDqDepth];   // weight of the entry in each ring slot
+#pragma unroll
+  for (int k = 0; k < kDqDepth - 1; ++k) gw[k] = issue_next(k);
   float acc[32];
 #pragma unroll
   for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-  for (int64_t j0 = 0; j0 < n; j0 += kDqRing) {
+  for (int64_t j0 = 0; j0 < n; j0 += kDqDepth) {
 #pragma unroll
-    for (int k = 0; k < kDqRing; ++k) {
-      const int64_t j = j0 + k;
-      if (j >= n) break;
-      // copy entry j + depth - 1 (its argmax fetched depth iterations ago)
-      const int kn = (k + kDqDepth - 1) % kDqRing;
-      issue(j + kDqDepth - 1, ra[kn], (k + kDqDepth - 1) % kDqDepth);
-      cp_async_commit();
-      // fetch entry j + ring - 1 into the ring position entry j - 1 freed
-      const int kf = (k + kDqRing - 1) % kDqRing;
-      fetch(j + kDqRing - 1, ra[kf], rg[kf]);
-      cp_async_wait<kDqDepth - 1>();  // entry j's copies have landed
-      const float g = rg[k];
-      if (ra[k] >= 0) {
-        const uint8_t* src = dq_raw + (k % kDqDepth) * 4 * kDqThreads * 16 + tid * 16;
+    for (int k = 0; k < kDqDepth; ++k) {
+      if (j0 + k >= n) break;
+      gw[(k + kDqDepth - 1) % kDqDepth] = issue_next((k + kDqDepth - 1) % kDqDepth);   // entry j + depth - 1
+      cp_async_wait<kDqDepth - 1>();  // entry j's copies have landed (zeros if there was nothing to copy)
+      const float g = gw[k];
+      const uint8_t* src = dq_raw + k * 4 * kDqThreads * 16 + tid * 16;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src + v * kDqThreads * 16);
+      for (int v = 0; v < 4; ++v) {
+        const uint4 w = *reinterpret_cast<const uint4*>(src + v * kDqThreads * 16);
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float2 f = unpack2<T>(h == 0 ? w.x : h == 1 ? w.y : h == 2 ? w.z : w.w);
-            acc[v * 8 + 2 * h] = fmaf(g, f.x, acc[v * 8 + 2 * h]);
-            acc[v * 8 + 2 * h + 1] = fmaf(g, f.y, acc[v * 8 + 2 * h + 1]);
-          }
-        }
+        for (int h = 0; h < 4; ++h)
+          fma2(acc[v * 8 + 2 * h], acc[v * 8 + 2 * h + 1], g,
+               unpack2<T>(h == 0 ? w.x : h == 1 ? w.y : h == 2 ? w.z : w.w));
       }
     }
   }
@@ -449,7 +493,7 @@ template <typename T>
 maxsim_status launch_dq(const BwdParams& p, cudaStream_t stream) {
   const int R = dq_rows(p.d);
   const int blocks = p.nQ * ((p.nq + R - 1) / R);
-  const size_t dq_smem = dq_smem_bytes();
+  const size_t dq_smem = dq_smem_bytes(p.d);
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dq_smem));
   if (e == cudaSuccess) dq_kernel<T><<<dim3(blocks, p.splits), kDqThreads, dq_smem, stream>>>(p);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
@@ -501,7 +545,7 @@ maxsim_status launch_backward(const void* Q, int n_queries, int nq, int d, const
   p.nq = nq;
   p.d = d;
   p.nd = nd;
-  p.nq_shift = (nq & (nq - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(nq)) : -1;
+  p.nq_inv = nq > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + nq - 1) / nq) : 0u;   // nq <= 65536
   p.splits = backward_splits(B);
   p.partial = workspace;
   p.status = dev->status;

@@ -18,34 +18,30 @@
 // so one lane holds all of one query token's similarities and the maximum
 // over the document is a serial scan in that lane: no cross-lane reduction.
 // The MMA work on the padding rows is far below the tensor-core budget.
-// Roles (352 threads):
-//  * Producer (warp 8): one contiguous bulk copy per tile (rows x d int8: CSR
+// Roles (288 threads):
+//  * Producer (warp 6): one contiguous bulk copy per tile (rows x d int8: CSR
 //    rows are contiguous) into a ring of stages, no padding rows fetched, the
 //    tile's token scales beside it (4-byte cp.async per lane, arriving on the
 //    same stage barrier) and the tile's description (document, tile, rows,
 //    last-tile flag). It alone reads the CSR offsets, 32 documents at a time;
 //    a final stage marks the end of the CTA's work.
-//  * Converters (warps 4-7): int8 -> fp16 of each tile into one of two
+//  * Converters (warps 1, 2, 3, 5): int8 -> fp16 of each tile into one of two
 //    K-major, 128-byte-swizzled operand buffers. Per 4 bytes: an XOR makes
 //    them biased bytes u = x + 128, PRMT places each under the fp16 exponent
 //    of 1024 (value 1024 + u), and one packed fp16 subtract of 1152 gives x.
-//  * MMA (lane 0 of warps 9 and 10, alternate tiles): S^T = Q (M = 128) x
+//  * MMA (lane 0 of warps 7 and 8, alternate tiles): S^T = Q (M = 128) x
 //    D_tile^T (N = rows rounded up to 16) over K = d into one of four TMEM
 //    accumulators. Each issuing thread owns one operand buffer and two
 //    accumulators: a thread's barrier polls wait behind its own MMAs, and
 //    with two threads those are the tile before last, usually complete.
-//    The query's nq <= 32 rows are written into each of the four 32-row
-//    quarters of A, so every TMEM lane quarter holds the whole result.
-//  * Epilogue (warps 0-3, warp w reading TMEM lane quarter w = the query
-//    tokens): documents are dealt out by b mod 4, so all of a document's
-//    tiles meet in one warp's registers and the four warps scan on the four
-//    sub-partitions at once. Per tile each lane scans its row: one fp32
-//    multiply by the column's scale, strict-greater update in ascending
-//    token order (lowest token wins ties). At the document's last tile the
-//    lanes sum q_scale[i] * m_i and write the score and the per-token
-//    outputs. Warp 0 also writes documents without tiles (empty or
-//    rejected) as empty. Every epilogue warp walks every stage in order
-//    and releases it (the stage's empty barrier counts all four warps).
+//  * Epilogue (warps 0 and 4, both on TMEM lanes 0-31 = the query tokens):
+//    documents alternate between the two warps (by index parity), so all of
+//    a document's tiles meet in one warp's registers. Per tile each lane
+//    scans its row: one fp32 multiply by the column's scale, strict-greater
+//    update in ascending token order (lowest token wins ties). At the
+//    document's last tile the lanes sum q_scale[i] * m_i and write the score
+//    and the per-token outputs. Warp 0 also writes documents without tiles
+//    (empty or rejected) as empty.
 // Every wait is bounded (ptx.cuh); after a timeout the producer and the MMA
 // thread drain their asynchronous operations before the CTA exits.
 #include <cuda_runtime.h>
@@ -59,11 +55,9 @@
 namespace msim {
 namespace {
 
-constexpr int kTcEpiWarps = 4;     // warps 0-3: one per TMEM lane quarter
-constexpr int kTcConvWarp0 = 4;    // warps 4-7: converters
-constexpr int kTcProducerWarp = 8;
-constexpr int kTcMmaWarp = 9;      // and warp 10: the second MMA thread
-constexpr int kTcThreads = 32 * 11;
+constexpr int kTcThreads = 288;
+constexpr int kTcProducerWarp = 6;
+constexpr int kTcMmaWarp = 7;      // and warp 8: the second MMA thread
 constexpr int kTcRows = 128;       // document rows per tile (MMA N <= 128)
 constexpr int kTcM = 128;          // MMA M: query rows, nq <= 32 real
 constexpr int kTcAcc = 4;          // TMEM accumulators of kTcRows columns
@@ -364,8 +358,7 @@ template <bool DETAIL>
 __device__ void i8tc_epilogue(const I8TcParams& p, const I8TcSmem& sm, uint32_t tmem, int warp, int lane) {
   int64_t b0, b1;
   i8tc_range(p, b0, b1);
-  const int me = warp;                       // documents with (b & 3) == me
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lane quarter
+  const int me = warp >> 2;                  // documents with (b & 1) == me
   const uint32_t sbytes = stage_bytes_of(p.d);
   uint32_t acc = 0, cph = 0, slot = 0, sph = 0;
   int64_t next_b = b0;                       // warp 0: first document not yet written
@@ -383,7 +376,7 @@ __device__ void i8tc_epilogue(const I8TcParams& p, const I8TcSmem& sm, uint32_t 
       write_empty<DETAIL>(p, next_b, b, lane);
       next_b = b + 1;
     }
-    if (static_cast<int>(b & 3) == me) {
+    if (static_cast<int>(b & 1) == me) {
       if (t == 0) {
         bv = -INFINITY;
         bj = INT_MAX;
@@ -397,7 +390,7 @@ __device__ void i8tc_epilogue(const I8TcParams& p, const I8TcSmem& sm, uint32_t 
 #pragma unroll 1
       for (int c = 0; c * 32 < rows; ++c) {
         float v[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + acc * static_cast<uint32_t>(kTcRows) + 32 * c, v);
+        tmem_ld_32x32b_x32(tmem + acc * static_cast<uint32_t>(kTcRows) + 32 * c, v);
         const float4* sc4 = reinterpret_cast<const float4*>(sc + 32 * c);
         const int lim = rows - 32 * c;
 #pragma unroll
@@ -455,7 +448,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) i8tc_kernel(const I8TcParams p)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.S8; ++s) {
       mbar_init(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(sm.full8 + 8 * s)), 1 + 32);
-      mbar_init(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(sm.empty8 + 8 * s)), 32 * kTcEpiWarps);
+      mbar_init(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(sm.empty8 + 8 * s)), 64);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(sm.afull + 8 * i)), 128);
@@ -468,17 +461,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) i8tc_kernel(const I8TcParams p)
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
-  // the query, int8 -> fp16 in the K-major SW128 layout, written into each of
-  // the four 32-row quarters of the M = 128 operand (rows 32 w + i = Q[i],
-  // rows past nq zero): every TMEM lane quarter of an accumulator then holds
-  // all query tokens' similarities, and an epilogue warp on each of the four
-  // sub-partitions can scan a tile
+  // the query, int8 -> fp16 in the K-major SW128 layout (rows past nq zero)
   {
     const int n = kTcM * D16;
     for (int i = threadIdx.x; i < n; i += kTcThreads) {
-      const int r = i / D16, ci = i - r * D16, qi = r & 31;
+      const int r = i / D16, ci = i - r * D16;
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (qi < p.nq) w = __ldg(reinterpret_cast<const uint4*>(p.Q + static_cast<int64_t>(qi) * p.d) + ci);
+      if (r < p.nq) w = __ldg(reinterpret_cast<const uint4*>(p.Q + static_cast<int64_t>(r) * p.d) + ci);
       cvt16(w, sm.q16, r, ci, kTcM * 128);
     }
     fence_proxy_async_smem();
@@ -492,10 +481,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) i8tc_kernel(const I8TcParams p)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
-  if (warp < kTcEpiWarps) {
+  if (warp == 0 || warp == 4) {
     i8tc_epilogue<DETAIL>(p, sm, tmem, warp, lane);
-  } else if (warp < kTcProducerWarp) {
-    i8tc_converter<D16>(p, sm, (warp - kTcConvWarp0) * 32 + lane);
+  } else if (warp <= 5) {
+    i8tc_converter<D16>(p, sm, (warp == 5 ? 3 : warp - 1) * 32 + lane);
   } else if (warp == kTcProducerWarp) {
     i8tc_producer(p, sm, lane);
   } else if (lane == 0) {
