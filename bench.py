@@ -166,7 +166,7 @@ class ClockSampler:
 class Headline:
     """Padded documents, optional length mask: configs 'colbert_*' and the d/Nd sweep."""
     kernel = "fwd_tc"
-    kernel_files = ("fwd_tc.cu", "ptx.cuh")
+    kernel_files = ("fwd_tc.cu", "fwd_common.cuh", "ptx.cuh")
 
     def __init__(self, args, device, rank):
         import maxsim_scoring_02_gb300 as m
@@ -193,9 +193,13 @@ class Headline:
             self.order_ms = 1e3 * (time.perf_counter() - t0)
         self.bound = "hbm"
         if self.dtype == "fp32":
-            # 16 FLOP per document byte against a ~12 FLOP/B FP32 ridge: the FMA pipe bounds it
-            self.kernel, self.kernel_files = "fwd_f32", ("fwd_f32.cu", "ptx.cuh")
-            self.bound, self.alu_unit = "alu", "ffma"
+            if self.d % 64 == 0 and self.nq <= 64 and (self.d // 64) * 3 * (32 if self.nq <= 32 else 64) * 128 <= 48 * 1024:
+                # tensor cores on three bf16 parts of each fp32 value: each fp32 byte read once, HBM-bound
+                self.kernel, self.kernel_files = "fwd_x3", ("fwd_x3.cu", "fwd_common.cuh", "ptx.cuh")
+            else:
+                # FFMA: 16 FLOP per document byte against a ~12 FLOP/B FP32 ridge, the FMA pipe bounds it
+                self.kernel, self.kernel_files = "fwd_f32", ("fwd_f32.cu", "ptx.cuh")
+                self.bound, self.alu_unit = "alu", "ffma"
         esz = _ELEM[self.dtype]
         tok = float(self.L.sum().item()) if self.L is not None else float(self.B * self.nd)
         # algorithmic bytes per launch: every real document token once, the query, one fp32 score per doc
@@ -264,7 +268,7 @@ def _lognormal_csr(w, B, seed, device):
 class Varlen:
     """Padding-free CSR documents, bf16 (B=500000 by default)."""
     kernel = "fwd_tc"
-    kernel_files = ("fwd_tc.cu", "ptx.cuh")
+    kernel_files = ("fwd_tc.cu", "fwd_common.cuh", "ptx.cuh")
     bound = "hbm"
 
     default_B = 500_000    # documents when --B is left at its default

@@ -171,7 +171,7 @@ maxsim_status maxsim_score(const void* Q, int n_queries, int nq, int d, const vo
   const int64_t rows = B * static_cast<int64_t>(nd);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == MAXSIM_FP32)
-    return launch_fwd_f32(static_cast<const float*>(Q), n_queries, nq, d, static_cast<const float*>(D), rows, 0,
+    return launch_fwd_fp32(static_cast<const float*>(Q), n_queries, nq, d, static_cast<const float*>(D), rows, 0,
                           doc_len, nullptr, B, nd, out, argmax_out, s);
   return launch_fwd_tc(Q, n_queries, nq, d, D, rows, 0, doc_len, nullptr, B, nd, dtype == MAXSIM_BF16 ? 1 : 0, out,
                        argmax_out, s);
@@ -244,7 +244,7 @@ maxsim_status maxsim_score_varlen(const void* Q, int n_queries, int nq, int d, c
   const int64_t rows = total_tokens > 0 ? total_tokens : 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == MAXSIM_FP32)
-    return launch_fwd_f32(static_cast<const float*>(Q), n_queries, nq, d, static_cast<const float*>(D_packed),
+    return launch_fwd_fp32(static_cast<const float*>(Q), n_queries, nq, d, static_cast<const float*>(D_packed),
                           total_tokens, 1, nullptr, offsets, B, 0, out, argmax_out, s);
   return launch_fwd_tc(Q, n_queries, nq, d, D_packed, rows, 1, nullptr, offsets, B, 0,
                        dtype == MAXSIM_BF16 ? 1 : 0, out, argmax_out, s);

@@ -44,6 +44,20 @@ maxsim_status launch_fwd_qm(const void* Q, int n_queries, int nq, int d, const v
                             int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
                             int is_bf16, float* out, int32_t* argmax, cudaStream_t stream);
 
+// Forward scoring with fp32 inputs on the tensor cores, each value split on
+// chip into three bf16 parts (one query of at most 64 tokens, d % 64 == 0,
+// the stacked query parts <= 48 KB); fwd_x3_applicable says whether it
+// takes a shape.
+bool fwd_x3_applicable(int n_queries, int nq, int d, int64_t total_rows);
+maxsim_status launch_fwd_x3(const float* Q, int nq, int d, const float* D, int64_t total_rows, int csr,
+                            const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd, float* out,
+                            int32_t* argmax, cudaStream_t stream);
+
+// fp32 forward: the tensor-core split kernel where it applies, else FFMA.
+maxsim_status launch_fwd_fp32(const float* Q, int n_queries, int nq, int d, const float* D, int64_t total_rows,
+                              int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,
+                              float* out, int32_t* argmax, cudaStream_t stream);
+
 // Forward scoring with fp32 inputs on the CUDA cores (FFMA).
 maxsim_status launch_fwd_f32(const float* Q, int n_queries, int nq, int d, const float* D, int64_t total_rows,
                              int csr, const int32_t* doc_len, const int64_t* offsets, int64_t B, int nd,

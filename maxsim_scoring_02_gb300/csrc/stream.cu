@@ -106,7 +106,7 @@ maxsim_status launch_streamed(const void* Q, int n_queries, int nq, int d, const
     float* o = n_queries == 1 ? out + b0 : otmp;
     int32_t* a = argmax ? (n_queries == 1 ? argmax + b0 * nq : atmp) : nullptr;
     const int32_t* L = doc_len_host ? lbuf[buf] : nullptr;
-    st = dtype == 2 ? launch_fwd_f32(static_cast<const float*>(Q), n_queries, nq, d,
+    st = dtype == 2 ? launch_fwd_fp32(static_cast<const float*>(Q), n_queries, nq, d,
                                      reinterpret_cast<const float*>(dbuf[buf]), nb * nd, 0, L, nullptr, nb, nd, o, a,
                                      stream)
                     : launch_fwd_tc(Q, n_queries, nq, d, dbuf[buf], nb * nd, 0, L, nullptr, nb, nd, dtype == 0 ? 1 : 0,

@@ -401,3 +401,42 @@ def test_multi_query_many_groups(nq):
     idx = torch.randperm(B, generator=torch.Generator().manual_seed(7))[:300].tolist() + [0, B - 1]
     Lc = L.cpu().numpy()
     _check_sampled(out.cpu().numpy(), am.cpu().numpy(), Q, lambda b: _np(D[b, :Lc[b]]), idx, P.TOL_LOWP)
+
+
+@pytest.mark.parametrize("nq,d,B,nd,csr", [
+    (32, 128, 500, 128, False),    # the configured shape: one 64-dim slice pair, four-slot tiles
+    (1, 64, 300, 70, False),       # one query token, one slice, ragged tiles
+    (20, 256, 200, 200, False),    # four slices, query rows past nq zero
+    (33, 128, 400, 129, False),    # 64-column query chunk (N = 192), a 1-row second tile
+    (64, 64, 157, 300, True),      # CSR, 64 query tokens
+    (32, 128, 3000, 40, True),     # many short CSR documents sharing tiles
+])
+def test_fp32_tensor_core_split(nq, d, B, nd, csr):
+    """fp32 inputs on the tensor cores: each value split into three bf16
+    parts, all nine part products accumulated in fp32. Scores within the
+    fp32 tolerance of the oracle, argmax by the near-tie rule; NaN and Inf in
+    the padding rows never reach a score."""
+    Q = workloads.normalized_tokens((nq, d), seed=nq * 7 + d, dtype="fp32")
+    D = workloads.normalized_tokens((B, nd, d), seed=B + nd + d, dtype="fp32")
+    L = workloads.uniform_lengths(B, 0, nd, seed=nq + d)
+    L[0], L[1], L[-1] = 0, 1, nd
+    if csr:
+        off = workloads.csr_offsets(L)
+        Dp = torch.cat([D[b, :L[b]] for b in range(B)])
+        out, am = m.maxsim_score_varlen(Q.to(DEV), Dp.to(DEV), off.to(DEV), want_argmax=True)
+    else:
+        j = torch.arange(nd)[None, :, None]
+        pad = j >= L.long()[:, None, None]
+        Dg = torch.where(pad & (j % 2 == 0), torch.full_like(D, float("nan")), D)
+        Dg = torch.where(pad & (j % 2 == 1), torch.full_like(D, float("inf")), Dg)
+        out, am = m.maxsim_score(Q.to(DEV), Dg.to(DEV), L.to(DEV), want_argmax=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    workloads.zero_padding(D, L)
+    Qn, Dn = _np(Q)[None], _np(D)
+    ref, ref_am, gap = oracle.maxsim(Qn, Dn, L.numpy(), want_gap=True)
+    P.check_scores(out.cpu().numpy(), ref, P.TOL_FP32)
+    eps = P.eps_rows(Qn, np.linalg.norm(Dn, axis=-1).max(axis=1), d)
+    P.check_argmax(am.cpu().numpy(), ref_am, gap, eps)
+    P.check_argmax_attains(am.cpu().numpy(), Qn, lambda b: Dn[b], ref_am, eps)
+    assert (out.cpu()[:, 0] == 0).all() and (am.cpu()[:, 0] == -1).all()
