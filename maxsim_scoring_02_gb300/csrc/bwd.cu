@@ -133,6 +133,7 @@ __device__ __forceinline__ void load_row_words(const void* src, uint32_t (&w)[DP
 // flight per lane to cover L2 latency, within the register budget of two
 // 16-warp CTAs per SM (64 registers a thread).
 __host__ __device__ constexpr int dd_batch(int dpl) { return dpl <= 4 ? 8 : dpl <= 8 ? 4 : dpl <= 16 ? 2 : 1; }
+// (for d <= 256 the batch is per half-warp: U entries of 2 * DPL values each)
 
 __host__ __device__ constexpr size_t dd_smem_bytes(int nw, int nd, int nQ, int ne) {
   return (static_cast<size_t>(nd) + 1 + nQ + nw) * 4 + (static_cast<size_t>(nw) * nd + 2 * static_cast<size_t>(ne)) * 2;
@@ -235,39 +236,80 @@ __global__ void __launch_bounds__(NW * 32, 2) dd_kernel(const BwdParams p) {
       __syncwarp();
     }
     __syncthreads();
-    // destination-owned rows: warp per row j of dD[b]. Up to U entries' Q rows
-    // are loaded together (their FMAs then run in list order, which is
-    // ascending entry order: the sum does not depend on scheduling).
-    for (int j = warp; j < nd; j += NW) {
-      float acc[DPL];
+    // destination-owned rows: warp per row j of dD[b]; its entries' Q rows
+    // are loaded in batches (FMAs in list order within each batch lane), the
+    // sums are deterministic. Batches are branch-free: one running past the
+    // row's last entry repeats that entry with weight 0 (its Q row is one the
+    // row adds anyway).
+    if constexpr (DPL <= 8) {
+      // d <= 256: each half-warp takes every other entry, lane l owning the
+      // 2 DPL dimensions [2 DPL (l % 16), ...) -- two entries per warp load,
+      // 16-byte loads at d = 128 -- and the halves add up at the row's end.
+      constexpr int DH = 2 * DPL;
+      const int half = lane >> 4;
+      const uint8_t* Qh = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(lane & 15) * DH * 2;
+      for (int j = warp; j < nd; j += NW) {
+        float acc[DH];
 #pragma unroll
-      for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-      const int r0 = rowptr[j], r1 = rowptr[j + 1];
-      // Branch-free batches: a batch running past the row's last entry repeats
-      // that entry with weight 0 (its Q row is one this row adds anyway).
-      for (int r = r0; r < r1; r += U) {
-        uint32_t x[U][DPL / 2];
-        float gq[U];
+        for (int k = 0; k < DH; ++k) acc[k] = 0.f;
+        const int r0 = rowptr[j], r1 = rowptr[j + 1];
+        for (int r = r0; r < r1; r += 2 * U) {
+          uint32_t x[U][DH / 2];
+          float gq[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int e = list[min(r + u, r1 - 1)];
-          const float g = dsv[entry_query(p, e)];
-          gq[u] = r + u < r1 ? g : 0.f;
-          load_row_words<DPL>(Qb + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :] with e = q*nq + i
+          for (int u = 0; u < U; ++u) {
+            const int pos = r + 2 * u + half;
+            const int e = list[min(pos, r1 - 1)];
+            const float g = dsv[entry_query(p, e)];
+            gq[u] = pos < r1 ? g : 0.f;
+            load_row_words<DH>(Qh + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :], e = q*nq + i
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int k = 0; k < DH / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int k = 0; k < DH; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
+        if (half == 0) {
+          float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DH;
 #pragma unroll
-          for (int k = 0; k < DPL / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
+          for (int k = 0; k < DH; k += 4)
+            __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
+        }
       }
-      float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DPL;
-      if constexpr (DPL % 4 == 0) {
+    } else {
+      for (int j = warp; j < nd; j += NW) {
+        float acc[DPL];
 #pragma unroll
-        for (int k = 0; k < DPL; k += 4)
-          __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
-      } else {
+        for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+        const int r0 = rowptr[j], r1 = rowptr[j + 1];
+        // Branch-free batches: a batch running past the row's last entry repeats
+        // that entry with weight 0 (its Q row is one this row adds anyway).
+        for (int r = r0; r < r1; r += U) {
+          uint32_t x[U][DPL / 2];
+          float gq[U];
 #pragma unroll
-        for (int k = 0; k < DPL; k += 2) __stcs(reinterpret_cast<float2*>(drow + k), make_float2(acc[k], acc[k + 1]));
+          for (int u = 0; u < U; ++u) {
+            const int e = list[min(r + u, r1 - 1)];
+            const float g = dsv[entry_query(p, e)];
+            gq[u] = r + u < r1 ? g : 0.f;
+            load_row_words<DPL>(Qb + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :] with e = q*nq + i
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int k = 0; k < DPL / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
+        }
+        float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DPL;
+        if constexpr (DPL % 4 == 0) {
+#pragma unroll
+          for (int k = 0; k < DPL; k += 4)
+            __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < DPL; k += 2) __stcs(reinterpret_cast<float2*>(drow + k), make_float2(acc[k], acc[k + 1]));
+        }
       }
     }
     __syncthreads();
