@@ -20,6 +20,7 @@
 namespace msim {
 namespace {
 
+
 // Two groups of four slot-partial warps take tiles round-robin (warp w reads
 // TMEM lane quarter w % 4); then the producer, MMA and merge warps.
 constexpr int kGroups = 2;
@@ -31,6 +32,11 @@ constexpr int kCapSlots = 256;       // chunk slots per group table
 constexpr int kCapDocs = 256;        // documents per group table
 constexpr int kMaxAcc = 4;
 constexpr int kMaxFin = 5;           // documents finished per tile (4 slots + pass end)
+// slot_doc entries: bits 0-15 the local document index; bit 16 set when all
+// the document's slots lie in this slot's tile (it starts and ends there), in
+// which case bits 17-19 hold its slot count and the partial warps finish it.
+constexpr int kSlotLocal = 1 << 16;
+constexpr int kSlotDocMask = 0xffff;
 
 struct FwdTcParams {
   const int32_t* order;     // walk position -> document index, or null (identity)
@@ -49,6 +55,7 @@ struct FwdTcParams {
   int n_acc;
   int n_qslots;
   int n_part;      // slot-partial buffers between the partial warps and the merge warp
+  int local_finish;  // single pass: the partial warps finish documents whose slots lie in one tile
   uint32_t idesc;
   uint32_t tmem_cols;
   float* out;
@@ -63,7 +70,7 @@ struct GroupTab {
   int64_t first_doc;       // global index of local document 0
   int32_t slot_row[kCapSlots];   // first row of the chunk in D
   int32_t slot_info[kCapSlots];  // (chunk index in doc << 6) | valid rows (1..32)
-  int32_t slot_doc[kCapSlots];   // local document index
+  int32_t slot_doc[kCapSlots];   // local document index and flags (kSlotLocal)
   int32_t doc_len[kCapDocs];     // 0 for empty (or rejected) documents
 };
 
@@ -115,12 +122,33 @@ __device__ void build_group(const FwdTcParams& p, GroupTab* T, int64_t& nb, int6
   int nslots = 0, ndocs = 0;
   if (lane == 0) T->first_doc = nb;
   const int64_t carry0 = carry;
-  while (nb < b1 && ndocs < kCapDocs && nslots < kCapSlots) {
+  // Round `it` of the loop below looks at documents nb0 + 32 * it + lane
+  // (every earlier round accepted 32); their descriptions are fetched up
+  // front, so the rounds wait for one global-load latency, not one each.
+  constexpr int kRounds = kCapDocs / 32;
+  const int64_t nb0 = nb;
+  int64_t pre_start[kRounds], pre_len[kRounds];
+  bool pre_bad[kRounds];
+#pragma unroll
+  for (int it = 0; it < kRounds; ++it) {
+    const int64_t b = nb0 + 32 * it + lane;
+    pre_start[it] = 0;
+    pre_len[it] = 0;
+    pre_bad[it] = false;
+    if (b < b1) pre_len[it] = doc_rows(p, b, pre_start[it], pre_bad[it]);
+  }
+#pragma unroll
+  for (int it = 0; it < kRounds; ++it) {
+    if (!(nb < b1 && ndocs < kCapDocs && nslots < kCapSlots)) break;
     const int64_t b = nb + lane;
     const bool in = b < b1 && ndocs + lane < kCapDocs;
     int64_t start = 0, L = 0;
     bool bad = false;
-    if (in) L = doc_rows(p, b, start, bad);
+    if (in) {
+      L = pre_len[it];
+      start = pre_start[it];
+      bad = pre_bad[it];
+    }
     if (bad) atomicOr(p.status, kDevErrBadInput);
     const int64_t ck0 = (lane == 0) ? carry : 0;   // chunks of this doc already placed
     int64_t chunks = in ? (L + kSlotRows - 1) / kSlotRows - ck0 : 0;
@@ -154,6 +182,9 @@ __device__ void build_group(const FwdTcParams& p, GroupTab* T, int64_t& nb, int6
     if (whole || split) {
       const int dl = ndocs + lane;
       T->doc_len[dl] = static_cast<int32_t>(L);
+      const int idx0 = nslots + pre;
+      const bool local = p.local_finish && whole && ck0 == 0 && placed > 0 && (idx0 >> 2) == ((idx0 + placed - 1) >> 2);
+      const int dflag = dl | (local ? (kSlotLocal | (placed << 17)) : 0);
       for (int k = 0; k < placed; ++k) {
         const int idx = nslots + pre + k;
         const int64_t ck = ck0 + k;
@@ -161,7 +192,7 @@ __device__ void build_group(const FwdTcParams& p, GroupTab* T, int64_t& nb, int6
         const int64_t left = L - ck * kSlotRows;
         T->slot_row[idx] = static_cast<int32_t>(rowk);
         T->slot_info[idx] = static_cast<int32_t>((ck << 6) | (left >= kSlotRows ? kSlotRows : left));
-        T->slot_doc[idx] = dl;
+        T->slot_doc[idx] = dflag;
       }
     }
     // totals (from the last placing lane)
@@ -291,33 +322,88 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
           if (!mbar_wait_a(br.partfull + 8 * pb, pph, sm.abort_flag, p.status)) return;
           const int i0 = 4 * t;
           const int nslot = min(4, n_slots - i0);
+          // one 16-byte read of the tile's four slot entries (i0 is a multiple of 4)
+          const int4 sd4 = *reinterpret_cast<const int4*>(T->slot_doc + i0);
+          const int sds[4] = {sd4.x, sd4.y, sd4.z, sd4.w};
+          bool any = cur >= 0;
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            if (w < nslot && !(sds[w] & kSlotLocal)) any = true;
           int nfin = 0;
           int64_t fin_doc[kMaxFin];
           float fin_sum[kMaxFin];
           const float* pv = sm.part_v + pb * 4 * NC;
           const int32_t* pi = sm.part_i + pb * 4 * NC;
-          for (int w = 0; w < nslot; ++w) {
-            const int64_t dg = first + T->slot_doc[i0 + w];
-            if (dg != cur) {
-              if (cur >= 0) fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, doc_at(p, cur), q));
-              cur = dg;
-#pragma unroll
-              for (int g = 0; g < NG; ++g) {
-                rm[g] = -INFINITY;
-                ra[g] = INT_MAX;
-              }
-            }
+          // a tile in the middle of the open document: fold its four slots
+          const bool through = nslot == 4 && sds[0] == sds[1] && sds[1] == sds[2] && sds[2] == sds[3] &&
+                               !(sds[0] & kSlotLocal) && first + (sds[0] & kSlotDocMask) == cur;
+          if (through) {
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
-              const float v2 = pv[w * NC + g * 32 + lane];
-              if (ARGMAX) {
-                const int i2 = pi[w * NC + g * 32 + lane];
-                if (v2 > rm[g] || (v2 == rm[g] && i2 < ra[g])) {
-                  rm[g] = v2;
-                  ra[g] = i2;
+              float v4[4];
+              int i4[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                v4[w] = pv[w * NC + g * 32 + lane];
+                i4[w] = ARGMAX ? pi[w * NC + g * 32 + lane] : 0;
+              }
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                if (ARGMAX) {
+                  if (v4[w] > rm[g] || (v4[w] == rm[g] && i4[w] < ra[g])) {
+                    rm[g] = v4[w];
+                    ra[g] = i4[w];
+                  }
+                } else {
+                  rm[g] = fmaxf(rm[g], v4[w]);
                 }
-              } else {
-                rm[g] = fmaxf(rm[g], v2);
+              }
+            }
+          } else if (any) {
+            // up to 64 query columns: all four slots' values first (independent
+            // loads), then the walk; wider chunks load in the walk
+            constexpr bool kPre = NG <= 2;
+            float sv[4][NG];
+            int si[4][NG];
+            if (kPre) {
+#pragma unroll
+              for (int w = 0; w < 4; ++w)
+#pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                  sv[w][g] = pv[w * NC + g * 32 + lane];
+                  si[w][g] = ARGMAX ? pi[w * NC + g * 32 + lane] : 0;
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              if (w < nslot) {
+                // slots of documents finished by the partial warps close the open document
+                const bool loc = (sds[w] & kSlotLocal) != 0;
+                const int64_t dg = loc ? -1 : first + (sds[w] & kSlotDocMask);
+                if (dg != cur) {
+                  if (cur >= 0) fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, doc_at(p, cur), q));
+                  cur = dg;
+#pragma unroll
+                  for (int g = 0; g < NG; ++g) {
+                    rm[g] = -INFINITY;
+                    ra[g] = INT_MAX;
+                  }
+                }
+                if (!loc) {
+#pragma unroll
+                  for (int g = 0; g < NG; ++g) {
+                    const float v2 = kPre ? sv[w][g] : pv[w * NC + g * 32 + lane];
+                    if (ARGMAX) {
+                      const int i2 = kPre ? si[w][g] : pi[w * NC + g * 32 + lane];
+                      if (v2 > rm[g] || (v2 == rm[g] && i2 < ra[g])) {
+                        rm[g] = v2;
+                        ra[g] = i2;
+                      }
+                    } else {
+                      rm[g] = fmaxf(rm[g], v2);
+                    }
+                  }
+                }
               }
             }
           }

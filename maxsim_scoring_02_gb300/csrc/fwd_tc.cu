@@ -14,9 +14,11 @@
 //    never loaded (TileMaxSim §5, the padding waste). Padded (length-masked)
 //    and CSR layouts only differ in where a document's rows start.
 //  * Persistent grid, one CTA per SM; CTA c owns a contiguous document range
-//    and walks it in groups of up to 256 chunks. The producer warp builds each
-//    group's slot table in shared memory (32 lanes load the document offsets
-//    in parallel), so no role waits on a global load in its issue loop.
+//    and walks it in groups of up to 256 chunks. A builder warp (warp 11)
+//    writes each group's slot table in shared memory one group ahead (32
+//    lanes load the document offsets of up to 256 documents at once), so no
+//    role waits on a global load in its issue loop and the loader keeps
+//    issuing copies across group boundaries.
 //  * Producer (warp 8, lane 0 issues): TMA loads of 64-dim x 32/128-row boxes,
 //    128-byte swizzled, into a ring of 16 KB stages; four contiguous slots go
 //    as one 128-row box. Every document byte is read from HBM once per
@@ -24,20 +26,29 @@
 //    the single pass of TileMaxSim §2(1) (BQ = Nq). With several queries or
 //    query chunks, all passes run over one group (<= 256 chunks) before the
 //    next, so the repeats are served by L2.
-//  * MMA (warp 9, lane 0 issues): tcgen05.mma kind::f16, M = 128 rows, N = NC
-//    query tokens, K = 16; every 64-wide d-slice of a tile accumulates into
-//    the same TMEM accumulator before any maximum is taken (TileMaxSim §2(2),
-//    dimension tiling). Up to four accumulators let it run ahead.
+//  * MMA (warp 9): tcgen05.mma kind::f16, M = 128 rows, N = NC query tokens,
+//    K = 16; every 64-wide d-slice of a tile accumulates into the same TMEM
+//    accumulator before any maximum is taken (TileMaxSim §2(2), dimension
+//    tiling). Up to four accumulators let it run ahead. The whole warp runs
+//    the issue loop and one elected lane issues each MMA: with the loop
+//    warp-uniform, issuing costs about half the cycles per MMA of a loop run
+//    by one lane alone.
 //  * Slot partials (warps 0-7, two groups of four taking tiles round-robin;
 //    warp w reads TMEM lane quarter w % 4): tcgen05.ld of 32 lanes, rows past
 //    the chunk's valid rows masked to -inf, a transpose butterfly of shuffles
 //    leaves lane l with the maximum (and lowest argmax) of query column l
-//    over the slot, handed over in a ring of shared-memory buffers.
-//  * Merge (warp 10): folds slot partials in document order and, when a
-//    document ends, sums its per-token maxima and writes the score
-//    (FLASH-MAXSIM Figure 1: only the scalar score is written). Partial
-//    warps never wait for the merge except through the buffer ring. The
-//    similarity tile exists only in TMEM and registers.
+//    over the slot, handed over in a ring of shared-memory buffers. A
+//    document whose slots all lie in one tile (every document of up to 128
+//    tokens that starts on a tile boundary, e.g. Nd = 32 / 64 / 128) is
+//    finished by the group itself: one of its slots' warps (in turn, tile by
+//    tile) folds its slots, sums the per-token maxima and writes the score;
+//    a one-slot document from registers, without waiting for the others.
+//  * Merge (warp 10): folds the slot partials of documents that span tiles,
+//    in document order, and when such a document ends sums its per-token
+//    maxima and writes the score (FLASH-MAXSIM Figure 1: only the scalar
+//    score is written). Partial warps never wait for the merge except
+//    through the buffer ring. The similarity tile exists only in TMEM and
+//    registers.
 //  * Every mbarrier wait is bounded (ptx.cuh); after an abort the producer
 //    drains its in-flight TMA loads and the MMA thread waits for its last MMA
 //    before TMEM is released.
@@ -53,6 +64,10 @@
 
 namespace msim {
 namespace {
+
+// The shared roles (fwd_common.cuh) plus a table-builder warp.
+constexpr int kBuilderWarp = kMergeWarp + 1;
+constexpr int kTcThreads = kThreads + 32;
 
 struct Smem {
   uint8_t* q;            // n_qslots x KB boxes of NC rows x 128 B
@@ -117,9 +132,36 @@ struct Bars {
   }
 };
 
+// ------------------------------------------------------------ table builder
+// Warp 11 builds each group's slot table (all 32 lanes) one group ahead of
+// the loader, so the loader never stops issuing copies to build one.
+__device__ void run_builder(const FwdTcParams& p, const Smem& sm, const Bars& br, int64_t b0, int64_t b1) {
+  const int lane = threadIdx.x & 31;
+  int64_t nb = b0, carry = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    const int buf = gi & 1;
+    GroupTab* T = sm.tab + buf;
+    if (gi >= 2) {
+      bool w = true;
+      if (lane == 0) w = mbar_wait_a(br.tabempty + 8 * buf, ((gi >> 1) - 1) & 1u, sm.abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) return;
+    }
+    const bool end = nb >= b1;
+    if (end) {
+      if (lane == 0) T->n_docs = -1;
+    } else {
+      build_group(p, T, nb, b1, carry);
+    }
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
+    if (end) return;
+  }
+}
+
 template <int NC>
 __device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& br, const CUtensorMap* tm_d128,
-                             const CUtensorMap* tm_d32, const CUtensorMap* tm_q, int64_t b0, int64_t b1) {
+                             const CUtensorMap* tm_d32, const CUtensorMap* tm_q) {
   const int lane = threadIdx.x & 31;
   // Test-only fault switch (maxsim_debug_set_faults): the loader issues
   // nothing, so every other role's bounded wait runs out and the CTA aborts
@@ -133,27 +175,16 @@ __device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& b
   int s = 0;
   uint32_t ph = 0, fills = 0, quse = 0;
   int prev_key = -1;
-  int64_t nb = b0, carry = 0;
   bool ok = true;
   for (uint32_t gi = 0; ok; ++gi) {
     const int buf = gi & 1;
-    GroupTab* T = sm.tab + buf;
-    if (gi >= 2) {
+    const GroupTab* T = sm.tab + buf;
+    {
       bool w = true;
-      if (lane == 0) w = mbar_wait_a(br.tabempty + 8 * buf, ((gi >> 1) - 1) & 1u, sm.abort_flag, p.status);
+      if (lane == 0) w = mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status);
       if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) { ok = false; break; }
     }
-    const bool end = nb >= b1;
-    if (end) {
-      if (lane == 0) T->n_docs = -1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
-      break;
-    }
-    build_group(p, T, nb, b1, carry);
-    __threadfence_block();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
+    if (T->n_docs < 0) break;
     if (lane == 0) {
       const int n_slots = T->n_slots;
       const int n_tiles = (n_slots + 3) >> 2;
@@ -210,6 +241,8 @@ __device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& b
       }
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive_a(br.tabempty + 8 * buf);   // slot rows read
   }
   if (!ok && lane == 0) {
     // After an abort: wait (bounded) for every load this warp may still have in flight.
@@ -221,8 +254,11 @@ __device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& b
 }
 
 // ----------------------------------------------------------------- MMA warp
+// The whole warp runs the issue loop (warp-uniform control flow); one
+// elected lane issues each MMA and commit.
 template <int NC>
 __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
+  const int lane = threadIdx.x & 31;
   const int S = p.stages, KB = p.KB, NQS = p.n_qslots, A = p.n_acc;
   const uint32_t idesc = p.idesc;
   const uint64_t adesc0 = sdesc_k_sw128(smem_u32(sm.stages));
@@ -232,7 +268,7 @@ __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, ui
   int prev_key = -1, slot = 0;
   for (uint32_t gi = 0;; ++gi) {
     const int buf = gi & 1;
-    if (!mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status)) break;
+    if (!__all_sync(0xffffffffu, mbar_wait_a(br.tabfull + 8 * buf, (gi >> 1) & 1u, sm.abort_flag, p.status))) break;
     const GroupTab* T = sm.tab + buf;
     if (T->n_docs < 0) break;
     const int n_tiles = (T->n_slots + 3) >> 2;
@@ -242,9 +278,9 @@ __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, ui
         if (n_tiles == 0) continue;
         const int key = q * p.n_chunks + c;
         if (key != prev_key) {
-          if (prev_key >= 0) umma_commit_a(br.qempty + 8 * slot);  // slot free once its MMAs retire
+          if (prev_key >= 0) umma_commit_el(br.qempty + 8 * slot);  // slot free once its MMAs retire
           slot = static_cast<int>(quse % NQS);
-          if (!mbar_wait_a(br.qfull + 8 * slot, (quse / NQS) & 1u, sm.abort_flag, p.status)) {
+          if (!__all_sync(0xffffffffu, mbar_wait_a(br.qfull + 8 * slot, (quse / NQS) & 1u, sm.abort_flag, p.status))) {
             ok = false;
             break;
           }
@@ -254,14 +290,14 @@ __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, ui
         }
         const uint64_t qdesc = qdesc0 + static_cast<uint64_t>((slot * KB * NC * 128) >> 4);
         for (int t = 0; t < n_tiles; ++t) {
-          if (!mbar_wait_a(br.accempty + 8 * a, aph ^ 1u, sm.abort_flag, p.status)) {
+          if (!__all_sync(0xffffffffu, mbar_wait_a(br.accempty + 8 * a, aph ^ 1u, sm.abort_flag, p.status))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * NC);
           for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait_a(br.full + 8 * s, ph, sm.abort_flag, p.status)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_a(br.full + 8 * s, ph, sm.abort_flag, p.status))) {
               ok = false;
               break;
             }
@@ -269,15 +305,15 @@ __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, ui
             const uint64_t ad = adesc0 + static_cast<uint64_t>(s * (kStageBytes >> 4));
             const uint64_t bd = qdesc + static_cast<uint64_t>((kb * NC * 128) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-            umma_commit_a(br.empty + 8 * s);  // stage reusable once these MMAs have read it
+            for (int kk = 0; kk < 4; ++kk) umma_f16_el(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_commit_el(br.empty + 8 * s);  // stage reusable once these MMAs have read it
             if (++s == S) {
               s = 0;
               ph ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit_a(br.accfull + 8 * a);  // accumulator ready for the epilogue
+          umma_commit_el(br.accfull + 8 * a);  // accumulator ready for the epilogue
           if (++a == A) {
             a = 0;
             aph ^= 1u;
@@ -286,10 +322,11 @@ __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, ui
       }
     }
     if (!ok) break;
-    mbar_arrive_a(br.tabempty + 8 * buf);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_a(br.tabempty + 8 * buf);
   }
-  // Wait until every MMA issued by this thread has completed before TMEM is freed.
-  umma_commit_a(br.done);
+  // Wait until every MMA issued by this warp has completed before TMEM is freed.
+  umma_commit_el(br.done);
   mbar_wait_drain(sm.bars + (br.done - br.full) / 8, 0, p.status);
 }
 
@@ -326,6 +363,8 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
         if (!mbar_wait_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
         tc_fence_after();
         const int i0 = 4 * t;
+        float own_v[NG];
+        int own_i[NG];
         if (quarter < n_slots - i0) {
           const int info = T->slot_info[i0 + quarter];
           const int vrows = info & 63;
@@ -350,6 +389,8 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
             warp_column_max<ARGMAX>(v, row, lane, bv, bi);
             pv[g * 32 + lane] = bv;
             if (ARGMAX) pi[g * 32 + lane] = bi;
+            own_v[g] = bv;
+            own_i[g] = bi;
           }
         } else {
           tc_fence_before();
@@ -357,6 +398,56 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
           if (lane == 0) mbar_arrive_a(br.accempty + 8 * a);
         }
         mbar_arrive_a(br.partfull + 8 * pb);  // every thread of the group arrives (count 128)
+        // A document whose slots all lie in this tile is finished here, by one
+        // of its slots' warps (taken in turn from tile to tile); a one-slot
+        // document by its own warp from registers, a longer one once the whole
+        // group has written its slots.
+        if (quarter < n_slots - i0) {
+          const int sd = T->slot_doc[i0 + quarter];
+          if (sd & kSlotLocal) {
+            const int info = T->slot_info[i0 + quarter];
+            const int ncs = (sd >> 17) & 7;
+            const int f0 = quarter - (info >> 6);            // the document's first slot in the tile
+            const int fin = ncs == 1 ? f0 : f0 + static_cast<int>((tt >> 1) % static_cast<uint32_t>(ncs));
+            if (quarter == fin) {
+              if (ncs > 1 && !mbar_wait_a(br.partfull + 8 * pb, pph, sm.abort_flag, p.status)) return;
+              const int64_t bd = doc_at(p, T->first_doc + (sd & kSlotDocMask));
+              float sum = 0.f;
+#pragma unroll
+              for (int g = 0; g < NG; ++g) {
+                float m = own_v[g];
+                int mi = own_i[g];
+                if (ncs > 1) {
+                  m = -INFINITY;
+                  mi = INT_MAX;
+                  for (int j = 0; j < ncs; ++j) {
+                    const int o = (pb * 4 + f0 + j) * NC + g * 32 + lane;
+                    const float v2 = sm.part_v[o];
+                    if (ARGMAX) {
+                      const int i2 = sm.part_i[o];
+                      if (v2 > m || (v2 == m && i2 < mi)) {
+                        m = v2;
+                        mi = i2;
+                      }
+                    } else {
+                      m = fmaxf(m, v2);
+                    }
+                  }
+                }
+                const int qc = g * 32 + lane;
+                if (qc < p.nq) {
+                  sum += m;
+                  if (ARGMAX && bd >= 0) p.argmax[bd * p.nq + qc] = mi;
+                }
+              }
+#pragma unroll
+              for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+              if (lane == 0 && bd >= 0) p.out[bd] = sum;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_a(br.partempty + 8 * pb);  // done reading this buffer
       }
     }
     __syncwarp();
@@ -365,7 +456,7 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
 }
 
 template <int NG, bool ARGMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_d128, const __grid_constant__ CUtensorMap tm_d32,
                   const __grid_constant__ CUtensorMap tm_q, const FwdTcParams p) {
   constexpr int NC = 32 * NG;
@@ -384,10 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + i, 1);          // accfull
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + p.n_acc + i, 4);  // accempty: the 4 warps of one group
     for (int i = 0; i < 2; ++i) mbar_init(rest + 4 + 2 * p.n_acc + i, 1);  // tabfull
-    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 4 * kGroups + 2);  // tabempty: MMA + partials + merge
+    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 4 * kGroups + 3);  // tabempty: loader + MMA + partials + merge
     uint64_t* pr = rest + 8 + 2 * p.n_acc;
     for (int i = 0; i < p.n_part; ++i) mbar_init(pr + i, 128);             // partfull: the threads of one group
-    for (int i = 0; i < p.n_part; ++i) mbar_init(pr + p.n_part + i, 1);    // partempty: merge warp
+    for (int i = 0; i < p.n_part; ++i) mbar_init(pr + p.n_part + i, 5);    // partempty: merge warp + the group's 4 warps
     mbar_init(pr + 2 * p.n_part, 1);                                       // done
     *sm.abort_flag = 0;
     fence_mbar_init();
@@ -410,9 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t b1 = (p.B * (blockIdx.x + 1)) / gridDim.x;
 
   if (warp == kProducerWarp) {
-    run_producer<NC>(p, sm, br, &tm_d128, &tm_d32, &tm_q, b0, b1);
+    run_producer<NC>(p, sm, br, &tm_d128, &tm_d32, &tm_q);
+  } else if (warp == kBuilderWarp) {
+    run_builder(p, sm, br, b0, b1);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma<NC>(p, sm, br, tmem_base);
+    run_mma<NC>(p, sm, br, tmem_base);
   } else if (warp == kMergeWarp) {
     run_merge<NG, ARGMAX>(p, sm, br);
   } else {
@@ -434,7 +527,7 @@ cudaError_t launch_variant(const CUtensorMap& d128, const CUtensorMap& d32, cons
   auto kern = fwd_tc_kernel<NG, ARGMAX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(d128, d32, tq, p);
+  kern<<<grid, kTcThreads, smem, stream>>>(d128, d32, tq, p);
   return cudaGetLastError();
 }
 
@@ -509,6 +602,7 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   p.KB = KB;
   p.n_chunks = n_chunks;
   p.multipass = multipass;
+  p.local_finish = multipass ? 0 : 1;
   p.stages = stages;
   p.n_acc = n_acc;
   p.n_qslots = n_qslots;
