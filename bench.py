@@ -383,9 +383,10 @@ class PQ:
 
 
 class I8:
-    """INT8 x INT8 scoring with per-token symmetric scales, d=128 (tcgen05, int8 -> fp16 on chip)."""
-    kernel = "i8tc"
-    kernel_files = ("i8tc.cu", "ptx.cuh")
+    """INT8 x INT8 scoring with per-token symmetric scales, d=128 (tcgen05, int8 -> fp16 on chip,
+    documents on the MMA's M dimension)."""
+    kernel = "fwd_i8x"
+    kernel_files = ("fwd_i8x.cu", "fwd_common.cuh", "i8_common.cuh", "ptx.cuh")
     bound = "hbm"
 
     default_B = 500_000    # documents when --B is left at its default

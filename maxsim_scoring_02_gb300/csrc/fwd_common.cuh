@@ -56,6 +56,8 @@ struct FwdTcParams {
   int n_qslots;
   int n_part;      // slot-partial buffers between the partial warps and the merge warp
   int local_finish;  // single pass: the partial warps finish documents whose slots lie in one tile
+  const float* col_scale;  // single pass, or null: the score sums col_scale[i] * m_i instead of m_i
+  const float* row_scale;  // per document row, or null: similarities are dot * row_scale[row]
   uint32_t idesc;
   uint32_t tmem_cols;
   float* out;
@@ -219,6 +221,34 @@ __device__ void build_group(const FwdTcParams& p, GroupTab* T, int64_t& nb, int6
   __syncwarp();
 }
 
+// ------------------------------------------------------------ table builder
+// A warp of its own builds each group's slot table (all 32 lanes) one group
+// ahead of the loader, so the loader never stops issuing copies to build one.
+template <class SmemT, class BarsT>
+__device__ void run_builder(const FwdTcParams& p, const SmemT& sm, const BarsT& br, int64_t b0, int64_t b1) {
+  const int lane = threadIdx.x & 31;
+  int64_t nb = b0, carry = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    const int buf = gi & 1;
+    GroupTab* T = sm.tab + buf;
+    if (gi >= 2) {
+      bool w = true;
+      if (lane == 0) w = mbar_wait_a(br.tabempty + 8 * buf, ((gi >> 1) - 1) & 1u, sm.abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) return;
+    }
+    const bool end = nb >= b1;
+    if (end) {
+      if (lane == 0) T->n_docs = -1;
+    } else {
+      build_group(p, T, nb, b1, carry);
+    }
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
+    if (end) return;
+  }
+}
+
 // Max over the 32 lanes of a warp for each of 32 columns: on return lane l
 // holds the maximum of column l (and, with ARGMAX, the lowest row index
 // attaining it). 31 shuffle rounds per value array.
@@ -274,12 +304,14 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
   int pb = 0;
   uint32_t pph = 0;
   int64_t cur = -1;
-  float rm[NG];
+  float rm[NG], qw[NG];
   int ra[NG];
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     rm[g] = -INFINITY;
     ra[g] = INT_MAX;
+    // weight of column g * 32 + lane in the score (single pass when scaled)
+    qw[g] = (p.col_scale && g * 32 + lane < p.nq) ? __ldg(p.col_scale + g * 32 + lane) : 1.f;
   }
   auto doc_sum = [&](int c, int64_t doc, int q) -> float {
     float sum = 0.f;
@@ -287,7 +319,7 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
     for (int g = 0; g < NG; ++g) {
       const int qc = c * NC + g * 32 + lane;
       if (qc < p.nq) {
-        sum += rm[g];
+        sum += p.col_scale ? qw[g] * rm[g] : rm[g];
         if (ARGMAX && doc >= 0) p.argmax[(static_cast<int64_t>(q) * p.B + doc) * p.nq + qc] = ra[g];
       }
     }
@@ -417,7 +449,24 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
             fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, doc_at(p, cur), q));
             cur = -1;
           }
-          if (nfin > 0) {
+          auto write_doc = [&](int64_t b, float total) {   // b is a walk position
+            const int64_t bd = doc_at(p, b);
+            const int64_t o = static_cast<int64_t>(q) * p.B + bd;
+            if (p.n_chunks == 1) {
+              if (bd >= 0) p.out[o] = total;
+            } else {
+              const int dl = static_cast<int>(b - first);
+              const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
+              if (!last_chunk) sm.gsum[dl] = g2;
+              else if (bd >= 0) p.out[o] = g2;
+            }
+          };
+          if (nfin == 1) {   // the common case: one butterfly, lane 0 writes
+            float s = fin_sum[0];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) write_doc(fin_doc[0], s);
+          } else if (nfin > 1) {
 #pragma unroll
             for (int f = 0; f < kMaxFin; ++f)
               if (f < nfin) {
@@ -433,16 +482,7 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
                   total = fin_sum[f];
                   b = fin_doc[f];
                 }
-              const int64_t bd = doc_at(p, b);       // b is a walk position
-              const int64_t o = static_cast<int64_t>(q) * p.B + bd;
-              if (p.n_chunks == 1) {
-                if (bd >= 0) p.out[o] = total;
-              } else {
-                const int dl = static_cast<int>(b - first);
-                const float g2 = (c == 0 ? 0.f : sm.gsum[dl]) + total;
-                if (!last_chunk) sm.gsum[dl] = g2;
-                else if (bd >= 0) p.out[o] = g2;
-              }
+              write_doc(b, total);
             }
           }
         }

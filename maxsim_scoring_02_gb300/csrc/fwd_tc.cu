@@ -132,33 +132,6 @@ struct Bars {
   }
 };
 
-// ------------------------------------------------------------ table builder
-// Warp 11 builds each group's slot table (all 32 lanes) one group ahead of
-// the loader, so the loader never stops issuing copies to build one.
-__device__ void run_builder(const FwdTcParams& p, const Smem& sm, const Bars& br, int64_t b0, int64_t b1) {
-  const int lane = threadIdx.x & 31;
-  int64_t nb = b0, carry = 0;
-  for (uint32_t gi = 0;; ++gi) {
-    const int buf = gi & 1;
-    GroupTab* T = sm.tab + buf;
-    if (gi >= 2) {
-      bool w = true;
-      if (lane == 0) w = mbar_wait_a(br.tabempty + 8 * buf, ((gi >> 1) - 1) & 1u, sm.abort_flag, p.status);
-      if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) return;
-    }
-    const bool end = nb >= b1;
-    if (end) {
-      if (lane == 0) T->n_docs = -1;
-    } else {
-      build_group(p, T, nb, b1, carry);
-    }
-    __threadfence_block();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_a(br.tabfull + 8 * buf);
-    if (end) return;
-  }
-}
-
 template <int NC>
 __device__ void run_producer(const FwdTcParams& p, const Smem& sm, const Bars& br, const CUtensorMap* tm_d128,
                              const CUtensorMap* tm_d32, const CUtensorMap* tm_q) {
@@ -603,6 +576,8 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   p.n_chunks = n_chunks;
   p.multipass = multipass;
   p.local_finish = multipass ? 0 : 1;
+  p.col_scale = nullptr;
+  p.row_scale = nullptr;
   p.stages = stages;
   p.n_acc = n_acc;
   p.n_qslots = n_qslots;

@@ -572,6 +572,8 @@ maxsim_status launch_fwd_x3(const float* Q, int nq, int d, const float* D, int64
   p.n_chunks = 1;
   p.multipass = 0;
   p.local_finish = 0;
+  p.col_scale = nullptr;
+  p.row_scale = nullptr;
   p.stages = n_raw;      // raw fp32 stages
   p.n_acc = n_acc;
   p.n_qslots = n_op;     // bf16 operand stages

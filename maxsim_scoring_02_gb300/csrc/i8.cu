@@ -293,6 +293,9 @@ maxsim_status launch_i8(const int8_t* Q, const float* q_scale, int nq, int d, co
                         int32_t* maxdot, int32_t* argmax, cudaStream_t stream) {
   const DeviceInfo* dev = device_info();
   if (!dev) return MAXSIM_ERR_CUDA;
+  // scores only: documents on the tensor core's M dimension (exact dots)
+  if (!maxv && !maxdot && !argmax && i8x_applicable(nq, d, total_tokens))
+    return launch_i8x(Q, q_scale, nq, d, D, d_scale, offsets, B, total_tokens, out, stream);
   // d <= 256: the tcgen05 path (fp16 operands converted on chip, exact dots)
   if (i8tc_applicable(nq, d))
     return launch_i8tc(Q, q_scale, nq, d, D, d_scale, offsets, B, total_tokens, out, maxv, maxdot, argmax, stream);

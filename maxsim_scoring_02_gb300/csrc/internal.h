@@ -75,6 +75,12 @@ maxsim_status launch_i8(const int8_t* Q, const float* q_scale, int nq, int d, co
                         const int64_t* offsets, int64_t B, int64_t total_tokens, float* out, float* maxv,
                         int32_t* maxdot, int32_t* argmax, cudaStream_t stream);
 
+// INT8 x INT8 scores only, on tcgen05 with the documents on the MMA's M
+// dimension (int8 converted to fp16 on chip; exact for d <= 192).
+bool i8x_applicable(int nq, int d, int64_t total_tokens);
+maxsim_status launch_i8x(const int8_t* Q, const float* q_scale, int nq, int d, const int8_t* D, const float* d_scale,
+                         const int64_t* offsets, int64_t B, int64_t total_tokens, float* out, cudaStream_t stream);
+
 // INT8 x INT8 on tcgen05 (int8 converted to fp16 on chip; exact for d <= 256).
 bool i8tc_applicable(int nq, int d);
 maxsim_status launch_i8tc(const int8_t* Q, const float* q_scale, int nq, int d, const int8_t* D,
