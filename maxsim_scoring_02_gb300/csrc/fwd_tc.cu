@@ -14,27 +14,28 @@
 //    never loaded (TileMaxSim §5, the padding waste). Padded (length-masked)
 //    and CSR layouts only differ in where a document's rows start.
 //  * Persistent grid, one CTA per SM; CTA c owns a contiguous document range
-//    and walks it in groups of up to 256 chunks. A builder warp (warp 11)
-//    writes each group's slot table in shared memory one group ahead (32
-//    lanes load the document offsets of up to 256 documents at once), so no
+//    and walks it in groups of up to 256 chunks. A builder warp writes each
+//    group's slot table in shared memory one group ahead (32 lanes load the
+//    document offsets of up to 256 documents at once), so no
 //    role waits on a global load in its issue loop and the loader keeps
 //    issuing copies across group boundaries.
-//  * Producer (warp 8, lane 0 issues): TMA loads of 64-dim x 32/128-row boxes,
+//  * Loader (one lane issues): TMA loads of 64-dim x 32/128-row boxes,
 //    128-byte swizzled, into a ring of 16 KB stages; four contiguous slots go
 //    as one 128-row box. Every document byte is read from HBM once per
 //    (query, query chunk) pass -- with one query of up to 256 tokens that is
 //    the single pass of TileMaxSim §2(1) (BQ = Nq). With several queries or
 //    query chunks, all passes run over one group (<= 256 chunks) before the
 //    next, so the repeats are served by L2.
-//  * MMA (warp 9): tcgen05.mma kind::f16, M = 128 rows, N = NC query tokens,
+//  * MMA warp: tcgen05.mma kind::f16, M = 128 rows, N = NC query tokens,
 //    K = 16; every 64-wide d-slice of a tile accumulates into the same TMEM
 //    accumulator before any maximum is taken (TileMaxSim §2(2), dimension
 //    tiling). Up to four accumulators let it run ahead. The whole warp runs
 //    the issue loop and one elected lane issues each MMA: with the loop
 //    warp-uniform, issuing costs about half the cycles per MMA of a loop run
 //    by one lane alone.
-//  * Slot partials (warps 0-7, two groups of four taking tiles round-robin;
-//    warp w reads TMEM lane quarter w % 4): tcgen05.ld of 32 lanes, rows past
+//  * Slot partials (warps 0 .. 4G-1, G = 2 or 3 groups of four taking tiles
+//    round-robin; warp w reads TMEM lane quarter w % 4; then come the loader,
+//    MMA, merge and builder warps): tcgen05.ld of 32 lanes, rows past
 //    the chunk's valid rows masked to -inf, a transpose butterfly of shuffles
 //    leaves lane l with the maximum (and lowest argmax) of query column l
 //    over the slot, handed over in a ring of shared-memory buffers. A
@@ -43,7 +44,7 @@
 //    finished by the group itself: one of its slots' warps (in turn, tile by
 //    tile) folds its slots, sums the per-token maxima and writes the score;
 //    a one-slot document from registers, without waiting for the others.
-//  * Merge (warp 10): folds the slot partials of documents that span tiles,
+//  * Merge warp: folds the slot partials of documents that span tiles,
 //    in document order, and when such a document ends sums its per-token
 //    maxima and writes the score (FLASH-MAXSIM Figure 1: only the scalar
 //    score is written). Partial warps never wait for the merge except
@@ -65,9 +66,14 @@
 namespace msim {
 namespace {
 
-// The shared roles (fwd_common.cuh) plus a table-builder warp.
-constexpr int kBuilderWarp = kMergeWarp + 1;
-constexpr int kTcThreads = kThreads + 32;
+// Roles by warp index for G groups of four slot-partial warps (warps
+// 0 .. 4G-1): then the loader, the MMA warp, the merge warp and the table
+// builder. G = 3 when the partial warps bind (argmax, or d = 64 with
+// documents of at most 256 tokens), else 2.
+template <int G> struct TcRoles {
+  static constexpr int kLoader = 4 * G, kMma = 4 * G + 1, kMerge = 4 * G + 2, kBuilder = 4 * G + 3;
+  static constexpr int kThreads = 32 * (4 * G + 4);
+};
 
 struct Smem {
   uint8_t* q;            // n_qslots x KB boxes of NC rows x 128 B
@@ -307,14 +313,13 @@ __device__ void run_mma(const FwdTcParams& p, const Smem& sm, const Bars& br, ui
 // Warp w reduces slot w of every tile: TMEM lanes 32w..32w+31 hold 32 rows of
 // one document; the butterfly leaves the slot's per-column maxima in
 // part[pbuf][w][:], handed to the merge warp through partfull/partempty.
-template <int NG, bool ARGMAX>
+template <int NG, bool ARGMAX, int G>
 __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& br, uint32_t tmem_base) {
   constexpr int NC = 32 * NG;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;            // slot index == TMEM lane quarter
   const uint32_t grp = warp >> 2;          // groups take tiles round-robin
-  const int A = p.n_acc, PB = p.n_part;    // both powers of two
-  const int lgA = __ffs(A) - 1, lgPB = __ffs(PB) - 1;
+  const int A = p.n_acc, PB = p.n_part;    // both multiples of G
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
   uint32_t tt = 0;                         // global tile counter (same sequence as the MMA and merge)
   for (uint32_t gi = 0;; ++gi) {
@@ -327,11 +332,15 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
     const int passes = p.n_queries * p.n_chunks;
     for (int pass = 0; pass < passes; ++pass) {
       for (int t = 0; t < n_tiles; ++t, ++tt) {
-        if (tt % kGroups != grp) continue;
-        const int a = static_cast<int>(tt & static_cast<uint32_t>(A - 1));
-        const uint32_t aph = (tt >> lgA) & 1u;
-        const int pb = static_cast<int>(tt & static_cast<uint32_t>(PB - 1));
-        const uint32_t pph = (tt >> lgPB) & 1u;
+        if (tt % G != grp) continue;
+        // tile tt uses entry tt % n of a ring of n (n = A or PB, a multiple of
+        // G times a power of two): each entry is used by one group only, in
+        // that group's tile order, so no wait can run two phases ahead
+        const uint32_t tg = tt / G;
+        const int a = static_cast<int>(tt % G) + G * static_cast<int>(tg & static_cast<uint32_t>(A / G - 1));
+        const uint32_t aph = (tg >> (__ffs(A / G) - 1)) & 1u;
+        const int pb = static_cast<int>(tt % G) + G * static_cast<int>(tg & static_cast<uint32_t>(PB / G - 1));
+        const uint32_t pph = (tg >> (__ffs(PB / G) - 1)) & 1u;
         if (!mbar_wait_a(br.partempty + 8 * pb, pph ^ 1u, sm.abort_flag, p.status)) return;
         if (!mbar_wait_a(br.accfull + 8 * a, aph, sm.abort_flag, p.status)) return;
         tc_fence_after();
@@ -428,8 +437,8 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
   }
 }
 
-template <int NG, bool ARGMAX>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int NG, bool ARGMAX, int G>
+__global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_d128, const __grid_constant__ CUtensorMap tm_d32,
                   const __grid_constant__ CUtensorMap tm_q, const FwdTcParams p) {
   constexpr int NC = 32 * NG;
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + i, 1);          // accfull
     for (int i = 0; i < p.n_acc; ++i) mbar_init(rest + 4 + p.n_acc + i, 4);  // accempty: the 4 warps of one group
     for (int i = 0; i < 2; ++i) mbar_init(rest + 4 + 2 * p.n_acc + i, 1);  // tabfull
-    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 4 * kGroups + 3);  // tabempty: loader + MMA + partials + merge
+    for (int i = 0; i < 2; ++i) mbar_init(rest + 6 + 2 * p.n_acc + i, 4 * G + 3);  // tabempty: loader + MMA + partials + merge
     uint64_t* pr = rest + 8 + 2 * p.n_acc;
     for (int i = 0; i < p.n_part; ++i) mbar_init(pr + i, 128);             // partfull: the threads of one group
     for (int i = 0; i < p.n_part; ++i) mbar_init(pr + p.n_part + i, 5);    // partempty: merge warp + the group's 4 warps
@@ -456,12 +465,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kProducerWarp && lane == 0) {
+  if (warp == TcRoles<G>::kLoader && lane == 0) {
     tma_prefetch_desc(&tm_d128);
     tma_prefetch_desc(&tm_d32);
     tma_prefetch_desc(&tm_q);
   }
-  if (warp == kMmaWarp) {
+  if (warp == TcRoles<G>::kMma) {
     tmem_alloc(sm.tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
@@ -473,34 +482,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int64_t b0 = (p.B * blockIdx.x) / gridDim.x;
   const int64_t b1 = (p.B * (blockIdx.x + 1)) / gridDim.x;
 
-  if (warp == kProducerWarp) {
+  if (warp == TcRoles<G>::kLoader) {
     run_producer<NC>(p, sm, br, &tm_d128, &tm_d32, &tm_q);
-  } else if (warp == kBuilderWarp) {
+  } else if (warp == TcRoles<G>::kBuilder) {
     run_builder(p, sm, br, b0, b1);
-  } else if (warp == kMmaWarp) {
+  } else if (warp == TcRoles<G>::kMma) {
     run_mma<NC>(p, sm, br, tmem_base);
-  } else if (warp == kMergeWarp) {
+  } else if (warp == TcRoles<G>::kMerge) {
     run_merge<NG, ARGMAX>(p, sm, br);
   } else {
-    run_partials<NG, ARGMAX>(p, sm, br, tmem_base);
+    run_partials<NG, ARGMAX, G>(p, sm, br, tmem_base);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == TcRoles<G>::kMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
   }
 }
 
-template <int NG, bool ARGMAX>
+template <int NG, bool ARGMAX, int G>
 cudaError_t launch_variant(const CUtensorMap& d128, const CUtensorMap& d32, const CUtensorMap& tq,
                            const FwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
-  auto kern = fwd_tc_kernel<NG, ARGMAX>;
+  auto kern = fwd_tc_kernel<NG, ARGMAX, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kTcThreads, smem, stream>>>(d128, d32, tq, p);
+  kern<<<grid, TcRoles<G>::kThreads, smem, stream>>>(d128, d32, tq, p);
   return cudaGetLastError();
 }
 
@@ -534,12 +543,19 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   const int multipass = (n_queries * n_chunks > 1) ? 1 : 0;
   // multi-pass groups hold whole documents of at most 256 chunks
   if (multipass && !csr && nd > kCapSlots * kSlotRows) return MAXSIM_ERR_UNSUPPORTED;
-  const int n_acc = (512 / NC) < kMaxAcc ? (512 / NC) : kMaxAcc;
+  // Three groups of slot-partial warps where they bind (measured: argmax
+  // +10 %, d = 64 with Nd <= 256 +3-8 %), two elsewhere; with three, the
+  // accumulators and part buffers come in multiples of three (one set per
+  // group), so N <= 128.
+  const bool am = argmax != nullptr;
+  const bool g3 = (am || (KB == 1 && !csr && nd <= 256)) && NC <= 128;
+  const int G = g3 ? 3 : 2;
+  const int n_acc = g3 ? 3 * ((512 / NC) / 3 >= 2 ? 2 : 1) : ((512 / NC) < kMaxAcc ? (512 / NC) : kMaxAcc);
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(n_acc * NC)) tmem_cols <<= 1;
 
   const size_t budget = static_cast<size_t>(dev->max_smem_optin);
-  const int n_part = NC >= 128 ? 2 : 4;
+  const int n_part = g3 ? 3 : (NC >= 128 ? 2 : 4);
   int n_qslots = 1;
   if (multipass && smem_bytes_for(NC, KB, 4, n_acc, 2, n_part) <= budget) n_qslots = 2;
   int stages = 16;
@@ -590,17 +606,16 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
 
   const int grid = static_cast<int>(B < dev->sm_count ? B : dev->sm_count);
   cudaError_t e;
-  const bool am = argmax != nullptr;
+#define MAXSIM_TC_LAUNCH(NGv, AMv) \
+  (g3 ? launch_variant<NGv, AMv, 3>(tm_d128, tm_d32, tm_q, p, grid, smem, stream) \
+      : launch_variant<NGv, AMv, 2>(tm_d128, tm_d32, tm_q, p, grid, smem, stream))
   switch (NG) {
-    case 1: e = am ? launch_variant<1, true>(tm_d128, tm_d32, tm_q, p, grid, smem, stream)
-                   : launch_variant<1, false>(tm_d128, tm_d32, tm_q, p, grid, smem, stream); break;
-    case 2: e = am ? launch_variant<2, true>(tm_d128, tm_d32, tm_q, p, grid, smem, stream)
-                   : launch_variant<2, false>(tm_d128, tm_d32, tm_q, p, grid, smem, stream); break;
-    case 4: e = am ? launch_variant<4, true>(tm_d128, tm_d32, tm_q, p, grid, smem, stream)
-                   : launch_variant<4, false>(tm_d128, tm_d32, tm_q, p, grid, smem, stream); break;
-    default: e = am ? launch_variant<8, true>(tm_d128, tm_d32, tm_q, p, grid, smem, stream)
-                    : launch_variant<8, false>(tm_d128, tm_d32, tm_q, p, grid, smem, stream); break;
+    case 1: e = am ? MAXSIM_TC_LAUNCH(1, true) : MAXSIM_TC_LAUNCH(1, false); break;
+    case 2: e = am ? MAXSIM_TC_LAUNCH(2, true) : MAXSIM_TC_LAUNCH(2, false); break;
+    case 4: e = am ? MAXSIM_TC_LAUNCH(4, true) : MAXSIM_TC_LAUNCH(4, false); break;
+    default: e = am ? MAXSIM_TC_LAUNCH(8, true) : MAXSIM_TC_LAUNCH(8, false); break;
   }
+#undef MAXSIM_TC_LAUNCH
   return e == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
 }
 
