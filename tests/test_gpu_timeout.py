@@ -74,3 +74,40 @@ def test_wait_timeout_is_reported_and_the_next_call_is_correct(lib, layout):
 
 def test_unknown_fault_flags_are_rejected(lib):
     assert lib.maxsim_debug_set_faults(0x80, 0) == 1
+
+
+@pytest.mark.parametrize("kind", ["bf16_scores_only", "fp32_split", "i8_scores_only"])
+def test_wait_timeout_in_the_other_tensor_core_kernels(lib, kind):
+    """The same stall in the other pipelined kernels' loaders: the two-group
+    bf16 launch (scores only), the fp32 three-part kernel and the scores-only
+    INT8 kernel. Each reports MAXSIM_ERR_TIMEOUT and then scores exactly as
+    before."""
+    B, d = 300, 128
+    L = workloads.uniform_lengths(B, 0, 128, seed=911)
+    off = workloads.csr_offsets(L)
+    if kind == "i8_scores_only":
+        Qi, sq = workloads.quantize_int8(workloads.normalized_tokens((32, d), seed=912, dtype="fp32"))
+        Di, sd = workloads.quantize_int8(workloads.normalized_tokens((int(off[-1]), d), seed=913, dtype="fp32"))
+        args = (Qi.to(DEV), sq.to(DEV), Di.to(DEV), sd.to(DEV), off.to(DEV))
+        score = lambda: m.maxsim_score_i8(*args)
+    else:
+        dt = "bf16" if kind == "bf16_scores_only" else "fp32"
+        Q = workloads.normalized_tokens((32, d), seed=914, dtype=dt).to(DEV)
+        D = workloads.normalized_tokens((B, 128, d), seed=915, dtype=dt).to(DEV)
+        Ld = L.to(DEV)
+        score = lambda: m.maxsim_score(Q, D, Ld)
+
+    ref = score()
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    assert lib.maxsim_debug_set_faults(m.DEBUG_STALL_FWD_LOADER, 50_000_000) == 0
+    try:
+        score()
+        st, flags = m.maxsim_device_status()
+        assert st == TIMEOUT_STATUS and flags & m.DEVERR_TIMEOUT, (st, flags)
+    finally:
+        assert lib.maxsim_debug_set_faults(0, 0) == 0
+    out = score()
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    assert torch.equal(out, ref)
