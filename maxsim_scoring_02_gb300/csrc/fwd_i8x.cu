@@ -22,10 +22,11 @@
 //    (all d bytes of a row in one box row; one 128-row box for four
 //    contiguous slots, else one 32-row box per slot) into a ring of raw
 //    stages.
-//  * Converters (warps 12-15): int8 -> fp16 of each raw stage into a ring of
-//    operand stages, K-major with 128-byte swizzling (the exponent-bias
-//    conversion of i8_common.cuh), then release the raw stage. Reads of the
-//    raw stage are 16 contiguous bytes per thread (conflict-free).
+//  * Converters (warps 12-15): thread t converts tile row t of each raw
+//    stage into a ring of fp16 operand stages, K-major with 128-byte
+//    swizzling (the exponent-bias conversion of i8_common.cuh), walking the
+//    row's 16-byte chunks from chunk t mod 8 so that a quarter warp's reads
+//    and stores fall on distinct banks, then releases the raw stage.
 //  * MMA (warp 9, an elected lane issues): M = 128 document rows, N = 32 or
 //    64 query tokens, K = 16, d / 16 steps per tile into one of four TMEM
 //    accumulators.
@@ -64,7 +65,7 @@ constexpr int kI8xMaxRaw = 12, kI8xOp = 2;
 
 struct I8xSmem {
   uint8_t* q;            // KB slices x (NC rows x 128 B), fp16 swizzled
-  uint8_t* raw;          // p.stages x (128 rows x d bytes)
+  uint8_t* raw;          // p.stages x (128 rows x d bytes); d = 64: 64-byte swizzled
   uint8_t* op;           // p.n_qslots x (KB slices x 16 KB)
   GroupTab* tab;         // [2]
   uint64_t* bars;
@@ -192,20 +193,22 @@ __device__ void i8x_loader(const FwdTcParams& p, const I8xSmem& sm, const I8xBar
 }
 
 // ----------------------------------------------------------- converters
-// 128 threads; a raw stage is 128 rows x d bytes, row after row, cut into
-// 16-byte units: thread t converts units t, t + 128, ... (a warp reads 512
-// contiguous bytes at a time) into the operand stage's KB swizzled slices.
-// Each thread issues the loads of four or eight units before converting and
-// storing them, so the shared-memory load latency is paid once per batch.
+// Converter thread t (0..127) converts tile row t, 16 bytes (one chunk) at a
+// time, into two 16-byte chunks of the operand stage (K-major, 128-byte
+// swizzle). Thread t walks its row's n = d / 16 chunks starting at chunk
+// t mod 8 (d = 128, 192; at d = 64 the raw rows carry the 64-byte swizzle,
+// chunk j of row t at j ^ ((t >> 1) & 3), and every thread starts at 0), so
+// the eight rows of a quarter warp fall on distinct banks in the stores and
+// in the reads (two-way in the reads at d = 192). A thread loads its whole
+// row before it converts, releases the raw stage, then stores.
 template <int KB>
 __device__ void i8x_converters(const FwdTcParams& p, const I8xSmem& sm, const I8xBars& br) {
-  constexpr int kCpr = 4 * KB;                 // 16-byte units per row
-  constexpr int kPer = kCpr;                   // units per thread per stage: 128 rows x kCpr / 128 threads
-  constexpr int kBatch = kPer % 8 == 0 ? 8 : 4;
-  static_assert(kPer % kBatch == 0, "batching");
+  constexpr int kN = 4 * KB;                   // 16-byte chunks per row
   constexpr uint32_t kStage = 128u * 64u * KB, kOp = static_cast<uint32_t>(KB) * kI8xSlice;
   const int ct = threadIdx.x - 32 * kI8xConvWarp0, lane = threadIdx.x & 31;
-  const uint32_t raw0 = smem_u32(sm.raw), op0 = smem_u32(sm.op);
+  const int rot = KB == 1 ? 0 : (ct & 7);
+  const uint32_t sw = KB == 1 ? static_cast<uint32_t>((ct >> 1) & 3) : 0u;
+  const uint32_t row0 = smem_u32(sm.raw) + static_cast<uint32_t>(ct) * (64u * KB), op0 = smem_u32(sm.op);
   const int NR = p.stages, NO = p.n_qslots;
   int s = 0, o = 0;
   uint32_t ph = 0, oph = 0;
@@ -219,25 +222,26 @@ __device__ void i8x_converters(const FwdTcParams& p, const I8xSmem& sm, const I8
     const int n_tiles = (T->n_slots + 3) >> 2;
     for (int t = 0; t < n_tiles; ++t) {
       if (!mbar_wait_a(br.rawfull + 8 * s, ph, sm.abort_flag, p.status)) return;
+      const uint32_t src = row0 + static_cast<uint32_t>(s) * kStage;
+      uint4 w4[kN];
+#pragma unroll
+      for (int c = 0; c < kN; ++c) {
+        int j = c + rot;
+        if (j >= kN) j -= kN;
+        w4[c] = lds_u4(src + ((static_cast<uint32_t>(j) ^ sw) << 4));
+      }
+      mbar_arrive_a(br.rawempty + 8 * s);  // the row is in registers (the arrive orders the reads before it)
       if (!mbar_wait_a(br.opempty + 8 * o, oph ^ 1u, sm.abort_flag, p.status)) return;
-      const uint32_t src = raw0 + static_cast<uint32_t>(s) * kStage;
       const uint32_t dst = op0 + static_cast<uint32_t>(o) * kOp;
 #pragma unroll
-      for (int k0 = 0; k0 < kPer; k0 += kBatch) {
-        uint4 w4[kBatch];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) w4[k] = lds_u4(src + static_cast<uint32_t>(ct + 128 * (k0 + k)) * 16u);
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int u = ct + 128 * (k0 + k), r = u / kCpr, ci = u - r * kCpr;
-          cvt16(w4[k], dst, r, ci, kI8xSlice);
-        }
+      for (int c = 0; c < kN; ++c) {
+        int j = c + rot;
+        if (j >= kN) j -= kN;
+        cvt16(w4[c], dst, ct, j, kI8xSlice);
       }
-      // generic-proxy writes (read by the tensor core) and reads (the raw
-      // stage, next written by TMA) ordered before the async proxy's accesses
+      // generic-proxy writes, read by the tensor core, ordered before the async proxy's accesses
       fence_proxy_async_smem();
       mbar_arrive_a(br.opfull + 8 * o);    // every converter thread arrives after its own fence
-      mbar_arrive_a(br.rawempty + 8 * s);
       if (++s == NR) {
         s = 0;
         ph ^= 1u;
@@ -538,14 +542,15 @@ maxsim_status launch_i8x(const int8_t* Q, const float* q_scale, int nq, int d, c
   const size_t smem = i8x_smem_bytes(NC, d, n_raw, kI8xOp, n_acc, n_part);
   if (smem > budget) return MAXSIM_ERR_UNSUPPORTED;
 
-  // documents as a [total_tokens, d] uint8 matrix: boxes of d bytes (no
-  // swizzle) x 128 or 32 rows
+  // documents as a [total_tokens, d] uint8 matrix: boxes of d bytes x 128
+  // or 32 rows (64-byte swizzle at d = 64, none otherwise)
   alignas(64) CUtensorMap tm128, tm32;
   const uint64_t ddims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(total_tokens)};
   const uint64_t dstrides[1] = {static_cast<uint64_t>(d)};
   const uint32_t box128[2] = {static_cast<uint32_t>(d), 128}, box32[2] = {static_cast<uint32_t>(d), 32};
-  if (!encode_tmap(&tm128, 2, 2, const_cast<int8_t*>(D), ddims, dstrides, box128, 0) ||
-      !encode_tmap(&tm32, 2, 2, const_cast<int8_t*>(D), ddims, dstrides, box32, 0))
+  const int swz = d == 64 ? 2 : 0;
+  if (!encode_tmap(&tm128, 2, 2, const_cast<int8_t*>(D), ddims, dstrides, box128, swz) ||
+      !encode_tmap(&tm32, 2, 2, const_cast<int8_t*>(D), ddims, dstrides, box32, swz))
     return MAXSIM_ERR_CUDA;
 
   FwdTcParams p;
