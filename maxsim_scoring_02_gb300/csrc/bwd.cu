@@ -9,13 +9,15 @@
 // dd_kernel -- one CTA per document (persistent over documents). The
 // document's nQ*nq argmax entries are grouped by token j with a counting
 // sort in shared memory: each warp counts its chunk of entries into a
-// private histogram (lanes holding the same key are found with
-// __match_any_sync and only their leader updates the warp's counter, so no
+// private histogram (lanes holding the same key are found with one ballot
+// per key bit and only their lowest lane updates the warp's counter, so no
 // atomics are needed), a scan over (key, warp) gives the inverse CSR row
-// pointers, and a second pass scatters the entries stably. Then one warp per
-// destination row j sums dS * Q over its list in ascending entry order and
-// writes the row -- every row of dD[b] is written by exactly one warp, rows
-// nothing points at as zeros.
+// pointers, and a second pass scatters the entries stably. Then groups of
+// lanes (half-warps for d <= 256, else warps) each walk the sorted list over
+// their own contiguous range of rows, balanced by entries + rows, in batches
+// of entries that run across row boundaries; a row is written (zeros if
+// nothing points at it) once its last entry has been added -- every row of
+// dD[b] has exactly one writer and its entries are added in list order.
 //
 // dq_kernel -- each CTA owns a block of (q, i) destination rows; a thread
 // holds 32 dimensions of one row as fp32 accumulators in registers and sweeps
@@ -135,6 +137,19 @@ __device__ __forceinline__ void load_row_words(const void* src, uint32_t (&w)[DP
 __host__ __device__ constexpr int dd_batch(int dpl) { return dpl <= 4 ? 8 : dpl <= 8 ? 4 : dpl <= 16 ? 2 : 1; }
 // (for d <= 256 the batch is per half-warp: U entries of 2 * DPL values each)
 
+// Lanes of the warp whose key equals this lane's key, for keys below
+// 2^nbits (nbits warp-uniform): one ballot per key bit, keeping the lanes
+// that agree with this lane on that bit.
+__device__ __forceinline__ unsigned dd_peers(unsigned key, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int i = 0; i < nbits; ++i) {
+    const unsigned bit = (key >> i) & 1u;
+    const unsigned bal = __ballot_sync(0xffffffffu, bit != 0u);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
+}
+
 __host__ __device__ constexpr size_t dd_smem_bytes(int nw, int nd, int nQ, int ne) {
   return (static_cast<size_t>(nd) + 1 + nQ + nw) * 4 + (static_cast<size_t>(nw) * nd + 2 * static_cast<size_t>(ne)) * 2;
 }
@@ -157,6 +172,7 @@ __global__ void __launch_bounds__(NW * 32, 2) dd_kernel(const BwdParams p) {
   const int e_lo = warp * chunk, e_hi = min(ne, e_lo + chunk);
   const uint8_t* Qb = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(lane) * DPL * 2;
   const uint32_t qrow_bytes = static_cast<uint32_t>(p.d) * 2;   // e * qrow_bytes < 2^16 * 2^11
+  const int nbits = 32 - __clz(nd);                              // keys 0 .. nd
 
   for (int64_t b = blockIdx.x; b < p.B; b += gridDim.x) {
     int L = doc_length(p, b);
@@ -181,13 +197,13 @@ __global__ void __launch_bounds__(NW * 32, 2) dd_kernel(const BwdParams p) {
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kDevErrBadInput);
     __syncthreads();
-    // pass 1: per-warp histograms of the argmax keys
+    // pass 1: per-warp histograms of the argmax keys (key = token + 1, 0 = skip)
     for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
       const int e = e0 + lane;
-      const int key = e < e_hi ? static_cast<int>(keys[e]) - 1 : -1;
-      const unsigned grp = __match_any_sync(0xffffffffu, key);
-      if (key >= 0 && lane == __ffs(grp) - 1)
-        counts[warp * nd + key] = static_cast<uint16_t>(counts[warp * nd + key] + __popc(grp));
+      const unsigned key = e < e_hi ? keys[e] : 0u;
+      const unsigned grp = dd_peers(key, nbits);
+      if (key != 0u && lane == __ffs(grp) - 1)
+        counts[warp * nd + key - 1] = static_cast<uint16_t>(counts[warp * nd + key - 1] + __popc(grp));
       __syncwarp();
     }
     __syncthreads();
@@ -224,91 +240,97 @@ __global__ void __launch_bounds__(NW * 32, 2) dd_kernel(const BwdParams p) {
     // pass 2: stable scatter of entry ids into the inverse CSR list
     for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
       const int e = e0 + lane;
-      const int key = e < e_hi ? static_cast<int>(keys[e]) - 1 : -1;
-      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      const unsigned key = e < e_hi ? keys[e] : 0u;
+      const unsigned grp = dd_peers(key, nbits);
       int pos = 0;
-      if (key >= 0) pos = counts[warp * nd + key] + __popc(grp & ((1u << lane) - 1u));
+      if (key != 0u) pos = counts[warp * nd + key - 1] + __popc(grp & ((1u << lane) - 1u));
       __syncwarp();
-      if (key >= 0) {
+      if (key != 0u) {
         list[pos] = static_cast<uint16_t>(e);
-        if (lane == __ffs(grp) - 1) counts[warp * nd + key] = static_cast<uint16_t>(counts[warp * nd + key] + __popc(grp));
+        if (lane == __ffs(grp) - 1)
+          counts[warp * nd + key - 1] = static_cast<uint16_t>(counts[warp * nd + key - 1] + __popc(grp));
       }
       __syncwarp();
     }
     __syncthreads();
-    // destination-owned rows: warp per row j of dD[b]; its entries' Q rows
-    // are loaded in batches (FMAs in list order within each batch lane), the
-    // sums are deterministic. Batches are branch-free: one running past the
-    // row's last entry repeats that entry with weight 0 (its Q row is one the
-    // row adds anyway).
-    if constexpr (DPL <= 8) {
-      // d <= 256: each half-warp takes every other entry, lane l owning the
-      // 2 DPL dimensions [2 DPL (l % 16), ...) -- two entries per warp load,
-      // 16-byte loads at d = 128 -- and the halves add up at the row's end.
-      constexpr int DH = 2 * DPL;
-      const int half = lane >> 4;
-      const uint8_t* Qh = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(lane & 15) * DH * 2;
-      for (int j = warp; j < nd; j += NW) {
-        float acc[DH];
+    // Destination-owned rows. Entry groups of G lanes (half-warps for
+    // d <= 256, else warps), lane l of a group owning the DL dimensions
+    // [DL l, DL l + DL); group k walks the inverse CSR list over its own
+    // contiguous range of rows [ja, jb), cut so that entries + rows are
+    // balanced across groups, in batches of U entries that run across row
+    // boundaries. A row is written (zeros if nothing points at it) when its
+    // last entry has been added; its entries are added in list order, so the
+    // sums are deterministic and each row has exactly one writer.
+    {
+      constexpr int G = DPL <= 8 ? 16 : 32;
+      constexpr int DL = DPL * 32 / G;
+      constexpr int NG = NT / G;
+      const int grp = tid / G, sub = tid % G;
+      const uint8_t* Qs = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(sub) * DL * 2;
+      const int total = rowptr[nd];
+      // first row j with rowptr[j] + j >= k (total + nd) / NG (strictly increasing in j)
+      auto row_start = [&](int k) -> int {
+        if (k <= 0) return 0;
+        if (k >= NG) return nd;
+        const int64_t target = (static_cast<int64_t>(total + nd) * k) / NG;
+        int lo = 0, hi = nd;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (rowptr[mid] + mid >= target) hi = mid;
+          else lo = mid + 1;
+        }
+        return lo;
+      };
+      const int ja = row_start(grp), jb = row_start(grp + 1);
+      if (ja < jb) {
+        float acc[DL];
 #pragma unroll
-        for (int k = 0; k < DH; ++k) acc[k] = 0.f;
-        const int r0 = rowptr[j], r1 = rowptr[j + 1];
-        for (int r = r0; r < r1; r += 2 * U) {
-          uint32_t x[U][DH / 2];
+        for (int k = 0; k < DL; ++k) acc[k] = 0.f;
+        float* dbase = p.dD + b * nd * static_cast<int64_t>(p.d) + sub * DL;
+        int j = ja, pos = rowptr[ja], end = rowptr[ja + 1];
+        const int stop = rowptr[jb];
+        auto write_row = [&]() {   // row j is complete: write it and move to row j + 1
+          float* drow = dbase + static_cast<int64_t>(j) * p.d;
+          if constexpr (DL % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < DL; k += 4)
+              __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < DL; k += 2) __stcs(reinterpret_cast<float2*>(drow + k), make_float2(acc[k], acc[k + 1]));
+          }
+#pragma unroll
+          for (int k = 0; k < DL; ++k) acc[k] = 0.f;
+          ++j;
+        };
+        for (;;) {
+          while (pos == end) {   // rows whose lists are exhausted (or empty)
+            write_row();
+            if (j == jb) break;
+            end = rowptr[j + 1];
+          }
+          if (j == jb) break;
+          // pos < end <= stop: a batch of U entries from pos
+          uint32_t x[U][DL / 2];
           float gq[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const int pos = r + 2 * u + half;
-            const int e = list[min(pos, r1 - 1)];
-            const float g = dsv[entry_query(p, e)];
-            gq[u] = pos < r1 ? g : 0.f;
-            load_row_words<DH>(Qh + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :], e = q*nq + i
+            const int e = list[min(pos + u, stop - 1)];
+            gq[u] = dsv[entry_query(p, e)];
+            load_row_words<DL>(Qs + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :], e = q*nq + i
           }
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int k = 0; k < DH / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
-        }
-#pragma unroll
-        for (int k = 0; k < DH; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
-        if (half == 0) {
-          float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DH;
-#pragma unroll
-          for (int k = 0; k < DH; k += 4)
-            __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
-        }
-      }
-    } else {
-      for (int j = warp; j < nd; j += NW) {
-        float acc[DPL];
-#pragma unroll
-        for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-        const int r0 = rowptr[j], r1 = rowptr[j + 1];
-        // Branch-free batches: a batch running past the row's last entry repeats
-        // that entry with weight 0 (its Q row is one this row adds anyway).
-        for (int r = r0; r < r1; r += U) {
-          uint32_t x[U][DPL / 2];
-          float gq[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const int e = list[min(r + u, r1 - 1)];
-            const float g = dsv[entry_query(p, e)];
-            gq[u] = r + u < r1 ? g : 0.f;
-            load_row_words<DPL>(Qb + static_cast<uint32_t>(e) * qrow_bytes, x[u]);   // Q[q, i, :] with e = q*nq + i
+            if (pos + u < stop) {
+              while (pos + u == end) {   // entry pos + u opens a later row (stays below jb)
+                write_row();
+                end = rowptr[j + 1];
+              }
+#pragma unroll
+              for (int k = 0; k < DL / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
+            }
           }
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int k = 0; k < DPL / 2; ++k) fma2(acc[2 * k], acc[2 * k + 1], gq[u], unpack2<T>(x[u][k]));
-        }
-        float* drow = p.dD + (b * nd + j) * static_cast<int64_t>(p.d) + lane * DPL;
-        if constexpr (DPL % 4 == 0) {
-#pragma unroll
-          for (int k = 0; k < DPL; k += 4)
-            __stcs(reinterpret_cast<float4*>(drow + k), make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < DPL; k += 2) __stcs(reinterpret_cast<float2*>(drow + k), make_float2(acc[k], acc[k + 1]));
+          pos = min(pos + U, stop);
         }
       }
     }

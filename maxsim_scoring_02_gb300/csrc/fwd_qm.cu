@@ -15,8 +15,9 @@
 //  * Two TMEM accumulators (block pair j uses accumulator j % 2; a single
 //    block pair alternates between them), each 256 columns in both CTAs. TMEM lane = query row, column = document token, so
 //    the maximum over the document is thread-local (3-input max tree per
-//    32-column chunk); the argmax is searched only in a chunk that raises the
-//    running maximum. No similarity value leaves the SM.
+//    32-column chunk); the argmax is searched once per round of four chunks,
+//    in the first chunk holding the round's maximum, when that maximum
+//    raises the running one. No similarity value leaves the SM.
 //  * Eight epilogue warps per CTA: warps w and w + 4 share TMEM lane quarter
 //    w; the first four own the even block pairs (accumulator 0), the others
 //    the odd ones, so each accumulator has one in-order consumer per CTA and
@@ -452,23 +453,20 @@ __device__ __forceinline__ float qp_max32(const uint32_t (&r)[32]) {
   return fmaxf(cm, m2[3]);
 }
 
-// Lowest index x with value x equal to m (m is one of the 32 values).
-__device__ __forceinline__ int qp_first_eq(const uint32_t (&r)[32], float m) {
-  int idx = 31;
-#pragma unroll
-  for (int x = 31; x >= 0; --x)
-    if (__uint_as_float(r[x]) == m) idx = x;
-  return idx;
-}
-
 // Running maximum / argmax of one row over chunks [c_base, c_base + nc) of a
-// round held in r (columns past `valid` masked first).
+// round held in r (columns past `valid` masked first). The argmax is searched
+// once per round, and only when the round's maximum beats the running one:
+// in the first chunk whose maximum equals the round's (columns ascend, so this
+// is the lowest column holding it; ties with the running maximum keep the
+// earlier column), its values selected from the round by the chunk index.
 template <bool ARGMAX>
 __device__ __forceinline__ void qp_scan_round(uint32_t (&r)[kQpRound][32], int c_base, int nc, int valid,
                                               int col_base, float& rm, int& ra) {
+  float cm[kQpRound];
 #pragma unroll
   for (int c = 0; c < kQpRound; ++c) {
-    if (c >= nc) break;
+    cm[c] = -INFINITY;
+    if (c >= nc) continue;
     const int col0 = (c_base + c) * 32;
     if (col0 + 32 > valid) {
       const uint32_t ninf = __float_as_uint(-INFINITY);
@@ -476,11 +474,28 @@ __device__ __forceinline__ void qp_scan_round(uint32_t (&r)[kQpRound][32], int c
       for (int x = 0; x < 32; ++x)
         if (col0 + x >= valid) r[c][x] = ninf;
     }
-    const float cm = qp_max32(r[c]);
-    if (cm > rm) {  // columns ascend: strict > keeps the lowest index on ties
-      rm = cm;
-      if (ARGMAX) ra = col_base + col0 + qp_first_eq(r[c], cm);
+    cm[c] = qp_max32(r[c]);
+  }
+  static_assert(kQpRound == 4, "round of four chunks");
+  float rmax;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(rmax) : "f"(cm[0]), "f"(cm[1]), "f"(cm[2]));
+  rmax = fmaxf(rmax, cm[3]);
+  const bool better = rmax > rm;
+  if (!ARGMAX) {
+    if (better) rm = rmax;
+    return;
+  }
+  if (__any_sync(0xffffffffu, better) && better) {
+    const bool lo = !(cm[0] == rmax) && (cm[1] == rmax || !(cm[2] == rmax));   // first chunk: 1 or 3
+    const bool hi = !(cm[0] == rmax) && !(cm[1] == rmax);                     // first chunk: 2 or 3
+    int idx = 31;
+#pragma unroll
+    for (int x = 31; x >= 0; --x) {
+      const uint32_t v = hi ? (lo ? r[3][x] : r[2][x]) : (lo ? r[1][x] : r[0][x]);
+      if (__uint_as_float(v) == rmax) idx = x;
     }
+    rm = rmax;
+    ra = col_base + (c_base + (hi ? 2 : 0) + (lo ? 1 : 0)) * 32 + idx;
   }
 }
 
