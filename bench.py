@@ -825,6 +825,9 @@ def main():
     in_bytes = getattr(wl, "hbm_bytes", wl.bytes_per_launch)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if in_bytes < 4 * L2_BYTES else None
     if flush is not None:
+        # first touch of fresh device memory is slow (~0.2 s for 512 MB): do it before the timed region
+        flush.fill_(0)
+        torch.cuda.synchronize()
         wl.config = dict(wl.config, l2="inputs %.3f GB < 4 x L2: L2 flushed (512 MB write) before every step; "
                          "value from kernel time" % (in_bytes / 1e9))
     clocks = ClockSampler(local)
