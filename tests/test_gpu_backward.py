@@ -156,6 +156,37 @@ def test_backward_halves_equal_full_call():
     assert torch.equal(dQ1, dQ) and torch.equal(dD1, dD)
 
 
+@pytest.mark.parametrize("pattern", ["one_token", "heavy_tail", "even"])
+@pytest.mark.parametrize("d", [64, 128, 512])
+def test_dd_skewed_argmax(pattern, d):
+    """The inverse-CSR dD with skewed saved argmax: one token taking every
+    entry of a document, a heavy-tailed token distribution, and even tokens
+    only (odd rows get no entry), over empty, one-token and full-length
+    documents. The row ranges of the entry groups are cut by entries + rows,
+    so a single row can hold every entry of its document. dD matches the
+    oracle's dD for the same argmax, and every row no entry points at is
+    exactly zero."""
+    nQ, nq, B, nd = 2, 300, 40, 150
+    Q = workloads.normalized_tokens((nQ, nq, d), seed=801, dtype="bf16")
+    L = workloads.uniform_lengths(B, 0, nd, seed=802)
+    L[0], L[1], L[2] = 0, 1, nd
+    am = workloads.skewed_argmax(nQ, B, nq, L, pattern, seed=803)
+    dS = workloads.normal((nQ, B), seed=804)
+    dD = m.maxsim_backward_dd(Q.to(DEV), am.to(DEV), dS.to(DEV), nd, doc_len=L.to(DEV))
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    _, rD = oracle.backward(_np(Q), np.zeros((B, nd, d)), am.numpy(), dS.double().numpy(), L.numpy())
+    got = dD.cpu().numpy()
+    assert _rel(got, rD) <= REL
+    hit = np.zeros((B, nd), dtype=bool)
+    a = am.numpy()
+    for b in range(B):
+        v = a[:, b].ravel()
+        hit[b, v[v >= 0]] = True
+    assert (got[~hit] == 0).all()
+    assert hit[~(np.arange(nd)[None, :] < L.numpy()[:, None])].sum() == 0
+
+
 def _allreduce_worker(rank, world, port, part, q):
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))

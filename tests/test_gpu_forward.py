@@ -440,3 +440,32 @@ def test_fp32_tensor_core_split(nq, d, B, nd, csr):
     P.check_argmax(am.cpu().numpy(), ref_am, gap, eps)
     P.check_argmax_attains(am.cpu().numpy(), Qn, lambda b: Dn[b], ref_am, eps)
     assert (out.cpu()[:, 0] == 0).all() and (am.cpu()[:, 0] == -1).all()
+
+
+@pytest.mark.parametrize("nq", [32, 256])
+@pytest.mark.parametrize("K", [37, 200])
+def test_argmax_exact_ties_pick_the_first_occurrence(nq, K):
+    """Documents of 512 tokens built from K distinct tokens each: position t
+    of document b holds base token (3t + 5b) mod K, so every token recurs
+    across 32-row slots, 128-row tiles, 32-column chunks and rounds of four
+    chunks, and positions 0 .. K-1 are exactly the first occurrences. Equal
+    tokens give bit-identical similarities, so the argmax (lowest index among
+    exact ties) must lie below K. Its token must be the oracle's best token of
+    the base set wherever the best two differ by more than the fp32 bound.
+    nq = 32 runs the short-query kernel, nq = 256 the long-query one."""
+    d, nd, B = 128, 512, 64
+    base = workloads.normalized_tokens((B, K, d), seed=1201 + K, dtype="bf16")
+    pos = (3 * torch.arange(nd)[None, :] + 5 * torch.arange(B)[:, None]) % K       # [B, nd]
+    D = torch.gather(base, 1, pos[:, :, None].expand(B, nd, d))
+    Q = workloads.normalized_tokens((nq, d), seed=1202 + nq, dtype="bf16")
+    _, am = m.maxsim_score(Q.to(DEV), D.to(DEV), want_argmax=True)
+    torch.cuda.synchronize()
+    assert m.maxsim_device_status() == (0, 0)
+    am = am.cpu().numpy()[0]                                                       # [B, nq]
+    assert (am >= 0).all() and (am < K).all(), int((am >= K).sum())
+    _, ref_tok, gap = oracle.maxsim(Q[None].double().numpy(), base.double().numpy(), want_gap=True)
+    got_tok = np.take_along_axis(pos.numpy(), am, axis=1)
+    eps = P.eps_rows(Q[None].double().numpy(), np.ones(B), d)
+    sure = gap[0] >= eps[0]
+    assert sure.mean() > 0.9
+    assert (got_tok == ref_tok[0])[sure].all()

@@ -126,3 +126,30 @@ def sign_pattern_tokens(n: int, d: int, nnz: int, seed: int):
         r[idx] = sgn.to(torch.float64) * v
         rows.append(r)
     return torch.stack(rows)
+
+
+def skewed_argmax(n_queries: int, B: int, nq: int, lengths, pattern: str, seed: int):
+    """Argmax index tensors [n_queries, B, nq] (int32) with chosen token
+    distributions, as saved-forward inputs for the backward: every entry lies
+    in [0, L_b) for L_b > 0, and is -1 for empty documents.
+
+    pattern: "one_token" (every entry is token 0), "heavy_tail" (token
+    floor(L u^4), u ~ U[0,1): a few tokens take most entries), "even" (even
+    tokens only), "uniform"."""
+    g = _gen(seed, "cpu")
+    L = torch.as_tensor(lengths, dtype=torch.int64).view(1, B, 1)
+    u = torch.rand((n_queries, B, nq), generator=g, dtype=torch.float64)
+    Lf = L.to(torch.float64)
+    if pattern == "one_token":
+        a = torch.zeros((n_queries, B, nq), dtype=torch.int64)
+    elif pattern == "heavy_tail":
+        a = torch.floor(Lf * u ** 4).to(torch.int64)
+    elif pattern == "even":
+        a = 2 * torch.floor(torch.floor((Lf + 1) / 2) * u).to(torch.int64)
+    elif pattern == "uniform":
+        a = torch.floor(Lf * u).to(torch.int64)
+    else:
+        raise ValueError(pattern)
+    a = torch.minimum(a, (L - 1).clamp(min=0))
+    a = torch.where(L > 0, a, torch.full_like(a, -1))
+    return a.to(torch.int32)
