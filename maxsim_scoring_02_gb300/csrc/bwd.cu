@@ -101,9 +101,10 @@ __device__ __forceinline__ int doc_length(const BwdParams& p, int64_t b) {
 }
 
 // ------------------------------------------------------------------- dD
-// NW warps per CTA. DPL = d / 32 values per lane: lane l owns the DPL
-// consecutive dimensions [DPL l, DPL l + DPL) of a row, so one warp load of a
-// Q row is d * 2 contiguous bytes (whole 32-byte sectors).
+// NW warps per CTA; DPL = d / 32. The row walk takes entries in groups of
+// G lanes (16 for d <= 256, else 32); lane l of a group owns the DL =
+// 32 DPL / G consecutive dimensions [DL l, DL l + DL) of a row, so a group's
+// load of a Q row is d * 2 contiguous bytes (whole 32-byte sectors).
 
 // DPL 16-bit values at `src` (DPL * 2 bytes, aligned to that size up to 16)
 // as DPL / 2 packed 32-bit words.
@@ -131,11 +132,11 @@ __device__ __forceinline__ void load_row_words(const void* src, uint32_t (&w)[DP
   }
 }
 
-// Entries of one destination row gathered per batch: enough Q-row loads in
-// flight per lane to cover L2 latency, within the register budget of two
-// 16-warp CTAs per SM (64 registers a thread).
+// Entries gathered per batch of the row walk: enough Q-row loads in flight
+// per lane to cover L2 latency, within the register budget of two 16-warp
+// CTAs per SM (64 registers a thread). For d <= 256 the batch is per group
+// of 16 lanes: U entries of 2 DPL values each.
 __host__ __device__ constexpr int dd_batch(int dpl) { return dpl <= 4 ? 8 : dpl <= 8 ? 4 : dpl <= 16 ? 2 : 1; }
-// (for d <= 256 the batch is per half-warp: U entries of 2 * DPL values each)
 
 // Lanes of the warp whose key equals this lane's key, for keys below
 // 2^nbits (nbits warp-uniform): one ballot per key bit, keeping the lanes
@@ -170,7 +171,6 @@ __global__ void __launch_bounds__(NW * 32, 2) dd_kernel(const BwdParams p) {
   uint16_t* keys = list + ne;                                              // [ne] token + 1 (0 = skip)
   const int chunk = (ne + NW - 1) / NW;
   const int e_lo = warp * chunk, e_hi = min(ne, e_lo + chunk);
-  const uint8_t* Qb = static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(lane) * DPL * 2;
   const uint32_t qrow_bytes = static_cast<uint32_t>(p.d) * 2;   // e * qrow_bytes < 2^16 * 2^11
   const int nbits = 32 - __clz(nd);                              // keys 0 .. nd
 

@@ -549,7 +549,6 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
   // group), so N <= 128.
   const bool am = argmax != nullptr;
   const bool g3 = (am || (KB == 1 && !csr && nd <= 256)) && NC <= 128;
-  const int G = g3 ? 3 : 2;
   const int n_acc = g3 ? 3 * ((512 / NC) / 3 >= 2 ? 2 : 1) : ((512 / NC) < kMaxAcc ? (512 / NC) : kMaxAcc);
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(n_acc * NC)) tmem_cols <<= 1;
