@@ -12,7 +12,8 @@ oracle call; scores of the two launches are also compared with each other.
 Workloads (TileMaxSim deep reading §4: B, Nd and d scaling; §5: length mask
 and padding; FLASH-MAXSIM Abstract: variable-length CSR scoring):
   * Q[32,128] x D[500000,128,128] bf16, lengths U{32..128}, zero padding;
-  * the same at B = 100000 in fp16 and in fp32 (FFMA path);
+  * the same at B = 100000 and 500000 in fp16 and in fp32 (tcgen05 on three
+    bf16 parts of each fp32 value);
   * Q[32,768] x D[100000,512,768] bf16 and Q[32,64] x D[100000,32,64] bf16,
     full length (the corners of the d x Nd sweep);
   * Q[32,128] against 500000 CSR documents, lengths round(lognormal(ln 70,
@@ -102,9 +103,10 @@ def test_lenmask_b500k_bf16():
     _padded_case(500_000, 128, 128, "bf16", True)
 
 
+@pytest.mark.parametrize("B", [100_000, 500_000])
 @pytest.mark.parametrize("dtype", ["fp16", "fp32"])
-def test_lenmask_b100k(dtype):
-    _padded_case(100_000, 128, 128, dtype, True)
+def test_lenmask_fp16_fp32(dtype, B):
+    _padded_case(B, 128, 128, dtype, True)
 
 
 @pytest.mark.parametrize("nd,d", [(512, 768), (32, 64)])
