@@ -17,7 +17,7 @@ and padding; FLASH-MAXSIM Abstract: variable-length CSR scoring):
   * Q[32,768] x D[100000,512,768] bf16 and Q[32,64] x D[100000,32,64] bf16,
     full length (the corners of the d x Nd sweep);
   * Q[32,128] against 500000 CSR documents, lengths round(lognormal(ln 70,
-    0.5)) clipped to [8, 256], bf16.
+    0.5)) clipped to [8, 256], bf16 and fp32.
 """
 import math
 
@@ -114,14 +114,15 @@ def test_sweep_corners_b100k(nd, d):
     _padded_case(100_000, nd, d, "bf16", False)
 
 
-def test_csr_b500k_bf16():
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_csr_b500k(dtype):
     """bench.py Varlen workload, rank 0 (lengths seed 50, Q seed 51, D seed 52)."""
     B = 500_000
     L = workloads.lognormal_lengths(B, math.log(70), 0.5, 8, 256, seed=50, device=DEV)
     off = workloads.csr_offsets(L)
     T = int(off[-1].item())
-    Q = workloads.normalized_tokens((32, 128), seed=51, dtype="bf16", device=DEV)
-    Dp = workloads.normalized_tokens((T, 128), seed=52, dtype="bf16", device=DEV)
+    Q = workloads.normalized_tokens((32, 128), seed=51, dtype=dtype, device=DEV)
+    Dp = workloads.normalized_tokens((T, 128), seed=52, dtype=dtype, device=DEV)
     out_fast = m.maxsim_score_varlen(Q, Dp, off)
     out, am = m.maxsim_score_varlen(Q, Dp, off, want_argmax=True)
     torch.cuda.synchronize()
@@ -132,4 +133,4 @@ def test_csr_b500k_bf16():
     docs = np.zeros((len(idx), int(Lc[idx].max()), 128))
     for s, b in enumerate(idx):
         docs[s, :Lc[b]] = _np(Dp[offc[b]:offc[b + 1]])
-    _check(out_fast, out, am, _np(Q)[None], docs, Lc[idx], idx, P.TOL_LOWP)
+    _check(out_fast, out, am, _np(Q)[None], docs, Lc[idx], idx, P.TOL_FP32 if dtype == "fp32" else P.TOL_LOWP)
