@@ -295,10 +295,14 @@ __device__ __forceinline__ void fin_push(int64_t (&fd)[kMaxFin], float (&fs)[kMa
 // --------------------------------------------------------------- merge warp
 // Merges slot partials in document order (lane l owns query columns
 // l, l+32, ...), finishes documents (sum over query tokens, argmax), and
-// writes empty documents' outputs.
-template <int NG, bool ARGMAX, class SmemT, class BarsT>
+// writes empty documents' outputs. SINGLE: the launch is known to run one
+// query, one column chunk and one pass, and the other paths are compiled out.
+template <int NG, bool ARGMAX, bool SINGLE = false, class SmemT, class BarsT>
 __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br) {
   constexpr int NC = 32 * NG;
+  const int n_queries = SINGLE ? 1 : p.n_queries;
+  const int n_chunks = SINGLE ? 1 : p.n_chunks;
+  const bool multipass = SINGLE ? false : (p.multipass != 0);
   const int lane = threadIdx.x & 31;
   const int PB = p.n_part;
   int pb = 0;
@@ -334,9 +338,9 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
     const int n_slots = T->n_slots;
     const int n_tiles = (n_slots + 3) >> 2;
     const int64_t first = T->first_doc;
-    for (int q = 0; q < p.n_queries; ++q) {
-      for (int c = 0; c < p.n_chunks; ++c) {
-        const bool last_chunk = c == p.n_chunks - 1;
+    for (int q = 0; q < n_queries; ++q) {
+      for (int c = 0; c < n_chunks; ++c) {
+        const bool last_chunk = c == n_chunks - 1;
         // empty documents of the group: score 0, argmax -1 (no slots, no MMA)
         for (int dl = lane; dl < n_docs; dl += 32) {
           const int64_t b = doc_at(p, first + dl);
@@ -349,7 +353,7 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
             if (last_chunk) p.out[static_cast<int64_t>(q) * p.B + b] = 0.f;
           }
         }
-        if (p.multipass) cur = -1;
+        if (multipass) cur = -1;
         for (int t = 0; t < n_tiles; ++t) {
           if (!mbar_wait_a(br.partfull + 8 * pb, pph, sm.abort_flag, p.status)) return;
           const int i0 = 4 * t;
@@ -445,14 +449,14 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
             pb = 0;
             pph ^= 1u;
           }
-          if (p.multipass && t == n_tiles - 1 && cur >= 0) {
+          if (multipass && t == n_tiles - 1 && cur >= 0) {
             fin_push(fin_doc, fin_sum, nfin, cur, doc_sum(c, doc_at(p, cur), q));
             cur = -1;
           }
           auto write_doc = [&](int64_t b, float total) {   // b is a walk position
             const int64_t bd = doc_at(p, b);
             const int64_t o = static_cast<int64_t>(q) * p.B + bd;
-            if (p.n_chunks == 1) {
+            if (n_chunks == 1) {
               if (bd >= 0) p.out[o] = total;
             } else {
               const int dl = static_cast<int>(b - first);
@@ -492,7 +496,7 @@ __device__ void run_merge(const FwdTcParams& p, const SmemT& sm, const BarsT& br
     if (lane == 0) mbar_arrive_a(br.tabempty + 8 * buf);
   }
   // end of work: the last document of a single-pass walk is still open
-  if (!p.multipass && cur >= 0) {
+  if (!multipass && cur >= 0) {
     const int64_t bd = doc_at(p, cur);
     float sum = doc_sum(0, bd, 0);
 #pragma unroll

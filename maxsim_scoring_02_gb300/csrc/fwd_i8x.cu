@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kI8xThreads, 1)
   } else if (warp == kMmaWarp) {
     i8x_mma<NC>(p, sm, br, tmem_base);
   } else if (warp == kMergeWarp) {
-    run_merge<NG, false>(p, sm, br);
+    run_merge<NG, false, true>(p, sm, br);   // one query, one chunk, one pass
   } else if (warp == kI8xBuilderWarp) {
     run_builder(p, sm, br, b0, b1);
   } else if (warp >= kI8xConvWarp0) {
