@@ -437,7 +437,9 @@ __device__ void run_partials(const FwdTcParams& p, const Smem& sm, const Bars& b
   }
 }
 
-template <int NG, bool ARGMAX, int G>
+// SINGLE: one query, one column chunk, one pass (the merge's other paths
+// are compiled out).
+template <int NG, bool ARGMAX, int G, bool SINGLE = false>
 __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_d128, const __grid_constant__ CUtensorMap tm_d32,
                   const __grid_constant__ CUtensorMap tm_q, const FwdTcParams p) {
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
   } else if (warp == TcRoles<G>::kMma) {
     run_mma<NC>(p, sm, br, tmem_base);
   } else if (warp == TcRoles<G>::kMerge) {
-    run_merge<NG, ARGMAX>(p, sm, br);
+    run_merge<NG, ARGMAX, SINGLE>(p, sm, br);
   } else {
     run_partials<NG, ARGMAX, G>(p, sm, br, tmem_base);
   }
@@ -503,10 +505,10 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
   }
 }
 
-template <int NG, bool ARGMAX, int G>
+template <int NG, bool ARGMAX, int G, bool SINGLE = false>
 cudaError_t launch_variant(const CUtensorMap& d128, const CUtensorMap& d32, const CUtensorMap& tq,
                            const FwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
-  auto kern = fwd_tc_kernel<NG, ARGMAX, G>;
+  auto kern = fwd_tc_kernel<NG, ARGMAX, G, SINGLE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kern<<<grid, TcRoles<G>::kThreads, smem, stream>>>(d128, d32, tq, p);
@@ -608,8 +610,22 @@ maxsim_status launch_fwd_tc(const void* Q, int n_queries, int nq, int d, const v
 #define MAXSIM_TC_LAUNCH(NGv, AMv) \
   (g3 ? launch_variant<NGv, AMv, 3>(tm_d128, tm_d32, tm_q, p, grid, smem, stream) \
       : launch_variant<NGv, AMv, 2>(tm_d128, tm_d32, tm_q, p, grid, smem, stream))
+  // Scores-only launches of one query (up to 32 tokens), one chunk and one
+  // pass take the merge walk compiled for that case where documents end
+  // inside tiles or span them (CSR, length-masked, d = 64): measured +3 %
+  // length-masked and CSR, +9 % at d = 64 with 256-token documents. Full-length
+  // documents at d >= 128, the cheapest walk, measured ~1 % slower with it
+  // and keep the general build.
+  const bool single = !am && NG == 1 && n_queries == 1 && !multipass && p.n_chunks == 1 &&
+                      (csr || doc_len != nullptr || KB == 1);
   switch (NG) {
-    case 1: e = am ? MAXSIM_TC_LAUNCH(1, true) : MAXSIM_TC_LAUNCH(1, false); break;
+    case 1:
+      if (single)
+        e = g3 ? launch_variant<1, false, 3, true>(tm_d128, tm_d32, tm_q, p, grid, smem, stream)
+               : launch_variant<1, false, 2, true>(tm_d128, tm_d32, tm_q, p, grid, smem, stream);
+      else
+        e = am ? MAXSIM_TC_LAUNCH(1, true) : MAXSIM_TC_LAUNCH(1, false);
+      break;
     case 2: e = am ? MAXSIM_TC_LAUNCH(2, true) : MAXSIM_TC_LAUNCH(2, false); break;
     case 4: e = am ? MAXSIM_TC_LAUNCH(4, true) : MAXSIM_TC_LAUNCH(4, false); break;
     default: e = am ? MAXSIM_TC_LAUNCH(8, true) : MAXSIM_TC_LAUNCH(8, false); break;
