@@ -328,3 +328,43 @@ def test_backward_varlen_matches_padded():
     np.testing.assert_allclose(dD2, np.concatenate([dD[b, :L[b]] for b in range(4)]), rtol=0, atol=1e-12)
     for b in range(4):
         assert (dD[b, L[b]:] == 0).all()
+
+
+@pytest.mark.parametrize("pattern", ["one_token", "heavy_tail", "even", "uniform"])
+def test_skewed_argmax_generator(pattern):
+    """The saved-argmax generator used by the backward parity tests: entries
+    lie in [0, L_b) and are -1 exactly for empty documents; the patterns
+    have their stated shapes."""
+    L = np.array([0, 1, 2, 7, 64, 150, 33])
+    a = workloads.skewed_argmax(3, len(L), 200, L, pattern, seed=41).numpy()
+    assert a.shape == (3, len(L), 200) and a.dtype == np.int32
+    for b, l in enumerate(L):
+        if l == 0:
+            assert (a[:, b] == -1).all()
+        else:
+            assert ((a[:, b] >= 0) & (a[:, b] < l)).all()
+    live = a[:, L > 0]
+    if pattern == "one_token":
+        assert (live == 0).all()
+    if pattern == "even":
+        assert (live % 2 == 0).all()
+    if pattern == "heavy_tail":   # floor(L u^4): median ~ L/16 (9.4 here), against L/2 for uniform draws
+        assert np.median(a[:, 5]) <= 150 / 8
+
+
+def test_backward_one_token_argmax_closed_form():
+    """With every entry routed to token 0, dD[b, 0] = sum_q dS[q,b] sum_i
+    Q[q,i], every other row of dD is zero, and dQ[q,i] = sum_b dS[q,b] D[b,0]."""
+    rng = np.random.default_rng(43)
+    nQ, nq, B, nd, d = 2, 5, 4, 6, 8
+    Q = rng.standard_normal((nQ, nq, d))
+    D = rng.standard_normal((B, nd, d))
+    a = np.zeros((nQ, B, nq), dtype=np.int32)
+    dS = rng.standard_normal((nQ, B))
+    dQ, dD = oracle.backward(Q, D, a, dS)
+    for b in range(B):
+        np.testing.assert_allclose(dD[b, 0], sum(dS[q, b] * Q[q].sum(0) for q in range(nQ)), rtol=1e-12, atol=1e-12)
+        assert (dD[b, 1:] == 0).all()
+    for q in range(nQ):
+        for i in range(nq):
+            np.testing.assert_allclose(dQ[q, i], sum(dS[q, b] * D[b, 0] for b in range(B)), rtol=1e-12, atol=1e-12)
